@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Throughput of the fused exact-attention hot path on GB300.
+
+One step = one pass of the whole path: forward (O, LSE) then the
+recomputation backward (dQ, dK, dV) on the long-sequence workload
+B=2, H=16, N=8192, d=128, bf16, non-causal, scale 1/sqrt(128), with Gaussian
+inputs resident in HBM.  Credited FLOPs per step are the algorithm's
+matmuls only: forward 4*B*H*N^2*d, backward 2.5x that (halved for causal).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs its own copy of the workload (weak scaling:
+attention heads are independent problems, so no data-path collective); the
+timed region is bracketed by barriers and the max over ranks is taken.
+Prints exactly one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd / fwd+bwd TFLOP/s (bf16, N=8192, d=128) and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = {"workload": "exact attention fwd+bwd, B=2 H=16 N=8192 d=128 bf16 non-causal, "
+                        "scale 1/sqrt(128), Q/K/V/dO ~ N(0,1)",
+            "B": 2, "H": 16, "N": 8192, "d": 128, "causal": False, "dtype": "bf16",
+            "l2": "inputs larger than L2 (4 x 67 MB read per step; no explicit flush)"}
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def flops_per_step(B, H, N, d, causal):
+    fwd = 4.0 * B * H * N * N * d
+    if causal:
+        fwd /= 2.0
+    return fwd, 2.5 * fwd
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_heads(rank, world, B, H):
+    """Weak scaling: every rank owns a full, independent batch of B x H heads.
+    Returns the seed offset and the global index range of this rank's heads."""
+    per = B * H
+    return rank, (rank * per, (rank + 1) * per)
+
+
+def max_over_ranks(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "io_aware_exact_12_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel, config_key):
+    """DRAM bytes per launch from the committed ncu summary, only if it was
+    taken from the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    sha = sources_sha()
+    for ln in lines:
+        if ln.startswith("#") or not ln.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in ln.split() if "=" in tok)
+        if kv.get("kernel") == kernel and kv.get("config") == config_key and kv.get("sources_sha") == sha:
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in open(self.path).read().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def oracle_sample(N, d, causal, seed, heads=1):
+    """Times the float64 CPU oracle (forward + analytic backward, as it
+    stands) on `heads` heads of the workload.  Returns (seconds, credited
+    flops, threads)."""
+    import oracle
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+    x = make_inputs(AttnShape(1, heads, N, d), "bf16", seed=seed)
+    q, k, v, do = (x[n].double().numpy() for n in ("q", "k", "v", "do"))
+    scale = 1.0 / math.sqrt(d)
+    threads = oracle.default_threads()
+    oracle.build()
+    t0 = time.perf_counter()
+    o, _ = oracle.forward(q, k, v, scale, causal, threads=threads)
+    oracle.backward(q, k, v, o, do, scale, causal, threads=threads)
+    dt = time.perf_counter() - t0
+    f, b = flops_per_step(1, heads, N, d, causal)
+    return dt, f + b, threads
+
+
+def cpu_model():
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def run_reference(args):
+    """The oracle arm: the float64 CPU oracle timed on the host cores, each
+    step one head (of 32) of the same workload, forward + backward."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    N, d, causal = WORKLOAD["N"], WORKLOAD["d"], WORKLOAD["causal"]
+    times, fl, threads = [], 0.0, 1
+    for i in range(args.warmup + args.steps):
+        dt, fl, threads = oracle_sample(N, d, causal, seed=100 + i, heads=1)
+        if i >= args.warmup:
+            times.append(dt)
+    total = sum(times)
+    value = fl * len(times) / total / 1e12
+    sample = "1 of 32 heads (B=1, H=1, N=8192, d=128, non-causal) per step, forward + backward"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": dict(WORKLOAD),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample, "cpu": cpu_model()},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from io_aware_exact_12_gb300 import build as build_mod
+    if rank == 0 or not os.path.exists(build_mod.LIB_PATH):
+        build_mod.build()
+    barrier(world)
+    import io_aware_exact_12_gb300 as attn
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+
+    B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
+    scale = 1.0 / math.sqrt(d)
+    seed_off, _ = shard_heads(rank, world, B, H)
+    host = make_inputs(AttnShape(B, H, N, d), "bf16", seed=4 + seed_off)
+    q, k, v, do = (host[n].cuda() for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step(c=causal):
+        attn.attn_fwd(q, k, v, scale=scale, causal=c, o=o, lse=lse)
+        attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=c, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if attn.sync_status() != 0:
+        raise SystemExit("device status error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for i in range(K):
+            ev[i][0].record(stream)
+            attn.attn_fwd(q, k, v, scale=scale, causal=causal, o=o, lse=lse)
+            ev[i][1].record(stream)
+            attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=causal, dq=dq, dk=dk, dv=dv)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    status = attn.sync_status()
+    clk = clocks.summary()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    ms_step = max_over_ranks(total_ms / K, world)
+    f_fwd, f_bwd = flops_per_step(B, H, N, d, causal)
+    value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    launches = K * 4
+
+    # causal variant of the same workload (reported alongside, not in `value`)
+    cf_ms, cb_ms = [], []
+    for _ in range(2):
+        step(True)
+    for _ in range(max(K // 2, 3)):
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        attn.attn_fwd(q, k, v, scale=scale, causal=True, o=o, lse=lse)
+        e1.record(stream)
+        attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=True, dq=dq, dk=dk, dv=dv)
+        e2.record(stream)
+        torch.cuda.synchronize()
+        cf_ms.append(e0.elapsed_time(e1))
+        cb_ms.append(e1.elapsed_time(e2))
+    cf_f, cb_f = flops_per_step(B, H, N, d, True)
+
+    # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> host outputs
+    hin = {n: host[n].pin_memory() for n in ("q", "k", "v", "do")}
+    hout = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+
+    def e2e_step():
+        q.copy_(hin["q"], non_blocking=True)
+        k.copy_(hin["k"], non_blocking=True)
+        v.copy_(hin["v"], non_blocking=True)
+        do.copy_(hin["do"], non_blocking=True)
+        step()
+        hout["o"].copy_(o, non_blocking=True)
+        hout["lse"].copy_(lse, non_blocking=True)
+        hout["dq"].copy_(dq, non_blocking=True)
+        hout["dk"].copy_(dk, non_blocking=True)
+        hout["dv"].copy_(dv, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    s1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(s0.elapsed_time(s1) / K, world)
+    e2e_value = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
+    launches_e2e = K * 4
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    # dominant kernel: the one with the larger share of the step
+    if bwd_ms >= fwd_ms:
+        dom, dom_tf, dom_name = "attn_bwd_kernel", bwd_tf, "bwd"
+    else:
+        dom, dom_tf, dom_name = "attn_fwd_kernel", fwd_tf, "fwd"
+    traffic = traffic_from_profiles(dom, "c4_noncausal")
+    roof = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": peak, "unit": UNIT,
+            "frac": dom_tf / peak, "traffic": traffic, "peak_source": peak_src + " (burst bf16)",
+            "frac_of_sustained": dom_tf / peak_sus,
+            "note": ("bwd duration is the whole attn_bwd call (preprocess + main + dQ convert), "
+                     "so `achieved` understates the main kernel slightly") if dom_name == "bwd" else ""}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, threads = oracle_sample(N, d, causal, seed=4, heads=1)
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "1 of 32 heads (B=1, H=1, N=8192, d=128, non-causal), forward + backward, "
+                         "%.1f s" % dt, "cpu": cpu_model()}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": dict(WORKLOAD, parallelism="dp%d (independent heads per rank)" % world),
+                "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
+                "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak},
+                "causal": {"fwd_ms": statistics.median(cf_ms), "bwd_ms": statistics.median(cb_ms),
+                           "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
+                           "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
+                "roofline": roof, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches, "gpu_launches_e2e": launches_e2e,
+                "clocks": clk, "device_status": status}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

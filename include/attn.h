@@ -1,0 +1,116 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) fused exact-attention library.
+ *
+ * Exact scaled-dot-product attention, O = softmax(scale * Q K^T [+ causal
+ * mask]) V, computed as one fused tiled kernel that keeps the running row
+ * max m, running row sum l and an unnormalised O accumulator on chip, so the
+ * N x N score and probability matrices never reach HBM.  The forward stores
+ * O and the per-row log-sum-exp; the backward recomputes P from that LSE.
+ *
+ * Sources (web pages on FlashAttention):
+ *   - FlashAttention (PKM page), "三招": 1 Tiling, 2 Online Softmax (the m / l /
+ *     unnormalised-O recurrence and the final division by l), 3 Recomputation
+ *     (store O and the softmax statistics, rebuild P in the backward).
+ *   - FlashAttention深度攻略 (xiaohack page) §3 tiling into B_r query rows and
+ *     B_c key/value rows, §4 online-softmax derivation, §6 recomputation
+ *     backward, §7 kernel fusion, and the live-coding section whose module
+ *     works on a (B*H, N, d) view after transposing (B, N, H, d) inputs.
+ *   - "Flash Attention 到底做了什么？" (guanweilu page): exactness (differs from
+ *     the plain computation only in floating-point rounding order).
+ *
+ * Conventions shared by every call
+ *   - Tensors q, k, v, o, dO, dq, dk, dv are DEVICE pointers to contiguous
+ *     row-major [B, H, N, d] arrays of the call's element type (bf16 for the
+ *     unsuffixed calls, fp16 for the _f16 twins), 16-byte aligned.  This is
+ *     the (B*H, N, d) view of the pages' module; a caller holding (B, N, H, d)
+ *     tensors transposes first.
+ *   - lse is a DEVICE pointer to fp32 [B, H, N]: LSE_i = ln sum_j
+ *     exp(scale * q_i . k_j) over the keys visible to query i (natural log,
+ *     in the same units as the scaled logits).
+ *   - causal != 0 hides key j from query i iff j > i (square problem: query
+ *     and key positions share one index).  scale multiplies Q K^T as given.
+ *   - Supported: B, H, N >= 1; N <= 2^24; d in {32, 64, 128}; B*H <= 65535.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns; results are ready when the
+ *     stream is.  Calls on different streams that share outputs race.
+ *   - All memory passed in is owned by the caller.  The library keeps no
+ *     tensor between calls.  Outputs must not alias inputs.
+ *   - Errors: argument errors are returned synchronously (nothing is
+ *     enqueued).  A kernel that detects a problem on the device (a pipeline
+ *     wait that exceeded its time limit) records a sticky status that
+ *     attn_sync_status() returns; the kernel itself returns early instead of
+ *     hanging, and its outputs are then unspecified.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null/misaligned pointer, non-positive size, non-finite scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* head dim not in {32, 64, 128}, or sizes beyond the limits */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, allocation, ...) */
+  ATTN_ERR_TIMEOUT = 4,     /* a device-side pipeline wait gave up (sticky, see attn_sync_status) */
+  ATTN_ERR_ARCH = 5,        /* current device is not compute capability 10.3 (sm_103) */
+  ATTN_ERR_DEVICE_CHECK = 6 /* a kernel's own device-side check failed (sticky) */
+} attn_status_t;
+
+/*
+ * Forward pass, bf16 inputs/outputs, fp32 accumulation.
+ *   q, k, v : in,  [B, H, N, d] bf16
+ *   o       : out, [B, H, N, d] bf16, O = softmax(scale Q K^T [+mask]) V
+ *   lse     : out, [B, H, N] fp32, per-row log-sum-exp of the scaled logits
+ * Tiling / online softmax / final 1/l division: FlashAttention (PKM page)
+ * "三招" 1 and 2; FlashAttention深度攻略 §3-§4.
+ * Returns an attn_status_t.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Backward pass (recomputation), bf16.
+ *   q, k, v, o, dO : in, [B, H, N, d] bf16 (o is attn_fwd's output for q, k, v)
+ *   lse            : in, [B, H, N] fp32 from attn_fwd
+ *   dq, dk, dv     : out, [B, H, N, d] bf16 gradients of L = <O, dO>:
+ *                    P = exp(scale Q K^T - LSE) (rebuilt, never stored),
+ *                    D_i = sum_k dO_ik O_ik, dS = P o (dO V^T - D),
+ *                    dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
+ * Recomputation: FlashAttention (PKM page) "三招" 3; FlashAttention深度攻略 §6.
+ * Scratch: an fp32 dQ accumulator [B, H, N, d] and D [B, H, N] are taken
+ * from the stream-ordered allocator (cudaMallocAsync on `stream`) and freed
+ * on the same stream before the call returns (the memory is released when
+ * the stream reaches that point).
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             float scale, int causal, void* stream);
+
+/* fp16 twins: identical parameters and semantics with fp16 tensors. */
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, void* stream);
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the sticky device status of
+ * the current device (ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_DEVICE_CHECK), or
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+int attn_sync_status(void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char* attn_status_string(int status);
+
+/* Number of kernel launches the most recent successful attn_fwd* / attn_bwd*
+ * call on this thread enqueued (1 for the forward, 3 for the backward). */
+int attn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,147 @@
+"""GB300 (sm_103a) fused exact attention: Python binding of the C ABI in
+``include/attn.h``.
+
+This module only marshals arguments: it checks tensor shapes/dtypes, allocates
+outputs with torch (device memory and streams are the only things torch is
+used for), and calls the same-named C entry points of ``libattn.so`` through
+ctypes.  Every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or fails to load, every call
+raises.
+
+Layout: q, k, v, o, do and the gradients are contiguous [B, H, N, d] tensors
+(bf16 or fp16) on one CUDA device; lse is fp32 [B, H, N].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+__all__ = ["attn_fwd", "attn_bwd", "sync_status", "status_string", "last_launch_count", "lib",
+           "AttnError", "LIB_PATH", "STATUS"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+
+STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+          4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_ARCH", 6: "ATTN_ERR_DEVICE_CHECK"}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__("%s failed: %s (%d)" % (fn, STATUS.get(code, "?"), code))
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libattn.so not built; run `python -m io_aware_exact_12_gb300.build` "
+                              "(or __graft_entry__.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, I, P]
+        L.attn_fwd_f16.argtypes = L.attn_fwd.argtypes
+        L.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, P]
+        L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
+        for f in (L.attn_fwd, L.attn_fwd_f16, L.attn_bwd, L.attn_bwd_f16):
+            f.restype = I
+        L.attn_sync_status.argtypes = [P]
+        L.attn_sync_status.restype = I
+        L.attn_status_string.argtypes = [I]
+        L.attn_status_string.restype = ctypes.c_char_p
+        L.attn_last_launch_count.argtypes = []
+        L.attn_last_launch_count.restype = I
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().attn_status_string(int(code)).decode()
+
+
+def last_launch_count() -> int:
+    return lib().attn_last_launch_count()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _check(name, t, like=None, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous [B, H, N, d]" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s" % (name, dtype))
+    if like is not None and (t.shape != like.shape or t.device != like.device):
+        raise ValueError("%s must match q's shape/device" % name)
+
+
+def _dims(q):
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("q must be bf16 or fp16")
+    return tuple(int(x) for x in q.shape)
+
+
+def attn_fwd(q, k, v, scale=None, causal=False, o=None, lse=None, stream=None):
+    """O, LSE = exact softmax(scale q k^T [+ causal]) v.  Returns (o, lse)."""
+    B, H, N, d = _dims(q)
+    _check("q", q)
+    _check("k", k, q, q.dtype)
+    _check("v", v, q, q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("o", o, q, q.dtype)
+    _check("lse", lse, None, torch.float32)
+    fn = lib().attn_fwd if q.dtype == torch.bfloat16 else lib().attn_fwd_f16
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                float(scale), int(bool(causal)), _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_fwd", rc)
+    return o, lse
+
+
+def attn_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv=None, stream=None):
+    """dQ, dK, dV of L = <O, dO> by recomputation from LSE.  Returns (dq, dk, dv)."""
+    B, H, N, d = _dims(q)
+    _check("q", q)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(name, t, q, q.dtype)
+    _check("lse", lse, None, torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(name, t, q, q.dtype)
+    fn = lib().attn_bwd if q.dtype == torch.bfloat16 else lib().attn_bwd_f16
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_bwd", rc)
+    return dq, dk, dv
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the sticky device status."""
+    return lib().attn_sync_status(_stream_handle(stream))

@@ -1,0 +1,277 @@
+// attn_api.cu -- the C ABI declared in include/attn.h: argument validation,
+// tensor-map encoding, backward scratch, launch bookkeeping and the sticky
+// device status word.  Every step of the computation runs in the kernels of
+// attn_fwd.cu / attn_bwd.cu; this file only checks and marshals.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+// Sticky device-side status (one copy per device that loads the library).
+__device__ int g_attn_status;
+
+namespace attn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+thread_local int t_last_launches = 0;
+
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_arch_ok[kMaxDevices] = {};  // 0 unknown, 1 ok, -1 wrong arch
+cuuint64_t g_smem_attr_done[kMaxDevices][8] = {};
+const void* g_smem_attr_func[kMaxDevices][8] = {};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Current device, checked to be compute capability 10.3; returns a status.
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return kStatusCuda;
+  if (*dev < 0 || *dev >= kMaxDevices) return kStatusUnsupported;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_arch_ok[*dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess)
+      return kStatusCuda;
+    g_arch_ok[*dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return g_arch_ok[*dev] == 1 ? kStatusOk : kStatusArch;
+}
+
+int* status_ptr(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Checks shared by forward and backward.  Pure host logic: no CUDA call.
+int validate_common(int B, int H, int N, int d, float scale) {
+  if (B < 1 || H < 1 || N < 1) return kStatusInvalid;
+  if (!std::isfinite(scale)) return kStatusInvalid;
+  if (d != 32 && d != 64 && d != 128) return kStatusUnsupported;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  if (BH > 65535) return kStatusUnsupported;           // grid.y limit
+  if (N > (1 << 24)) return kStatusUnsupported;         // keeps row indices and TMA coords in range
+  return kStatusOk;
+}
+
+}  // namespace
+
+bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_inner,
+                     int box_rows, int row_bytes, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows),
+                             1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz =
+      row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool ensure_smem_attr(const void* func, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < 8; ++i) {
+    if (g_smem_attr_func[dev][i] == func && g_smem_attr_done[dev][i] >= (cuuint64_t)bytes) return true;
+  }
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  for (int i = 0; i < 8; ++i) {
+    if (g_smem_attr_func[dev][i] == nullptr || g_smem_attr_func[dev][i] == func) {
+      g_smem_attr_func[dev][i] = func;
+      g_smem_attr_done[dev][i] = static_cast<cuuint64_t>(bytes);
+      break;
+    }
+  }
+  return true;
+}
+
+BwdScratch bwd_scratch_layout(int BH, int N, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t Npad = static_cast<size_t>((N + 127) / 128) * 128;
+  BwdScratch s;
+  s.dq_off = 0;
+  s.lse2_off = up(static_cast<size_t>(BH) * N * d * sizeof(float));
+  s.d_off = s.lse2_off + up(static_cast<size_t>(BH) * Npad * sizeof(float));
+  s.total = s.d_off + up(static_cast<size_t>(BH) * Npad * sizeof(float));
+  return s;
+}
+
+namespace {
+
+int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+              int N, int d, float scale, int causal, void* stream, bool bf16) {
+  if (!q || !k || !v || !o || !lse) return kStatusInvalid;
+  int rc = validate_common(B, H, N, d, scale);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return kStatusInvalid;
+  const size_t nbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, nbytes, in, nbytes) || overlaps(lse, lbytes, in, nbytes)) return kStatusInvalid;
+  if (overlaps(o, nbytes, lse, lbytes)) return kStatusInvalid;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  int* st = status_ptr(dev);
+  if (!st) return kStatusCuda;
+  FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.BH = B * H; a.N = N; a.d = d;
+  a.sl2 = std::fabs(scale) * 1.4426950408889634f;
+  a.causal = causal ? 1 : 0;
+  a.negate = scale < 0.f ? 1 : 0;
+  a.bf16 = bf16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = st;
+  rc = launch_fwd(a);
+  if (rc == kStatusOk) t_last_launches = 1;
+  return rc;
+}
+
+int bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dO,
+              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+              float scale, int causal, void* stream, bool bf16) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return kStatusInvalid;
+  int rc = validate_common(B, H, N, d, scale);
+  if (rc) return rc;
+  for (const void* p : {q, k, v, o, dO, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    if (!aligned16(p)) return kStatusInvalid;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return kStatusInvalid;
+  const size_t nbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  for (const void* out : {static_cast<const void*>(dq), static_cast<const void*>(dk),
+                          static_cast<const void*>(dv)}) {
+    for (const void* in : {q, k, v, o, dO})
+      if (overlaps(out, nbytes, in, nbytes)) return kStatusInvalid;
+    if (overlaps(out, nbytes, lse, lbytes)) return kStatusInvalid;
+  }
+  if (overlaps(dq, nbytes, dk, nbytes) || overlaps(dq, nbytes, dv, nbytes) ||
+      overlaps(dk, nbytes, dv, nbytes))
+    return kStatusInvalid;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  int* st = status_ptr(dev);
+  if (!st) return kStatusCuda;
+  const BwdScratch lay = bwd_scratch_layout(B * H, N, d);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, lay.total, s) != cudaSuccess) return kStatusCuda;
+  BwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  a.BH = B * H; a.N = N; a.d = d;
+  a.sl2 = std::fabs(scale) * 1.4426950408889634f;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.negate = scale < 0.f ? 1 : 0;
+  a.bf16 = bf16;
+  a.stream = s;
+  a.status = st;
+  a.ws_dq = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.dq_off);
+  a.ws_lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.lse2_off);
+  a.ws_d = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.d_off);
+  rc = launch_bwd(a);
+  const cudaError_t fe = cudaFreeAsync(ws, s);
+  if (rc == kStatusOk && fe != cudaSuccess) rc = kStatusCuda;
+  if (rc == kStatusOk) t_last_launches = 3;
+  return rc;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int N, int d, float scale, int causal, void* stream) {
+  return attn::fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true);
+}
+
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, void* stream) {
+  return attn::fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, stream, false);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             float scale, int causal, void* stream) {
+  return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, true);
+}
+
+int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, void* stream) {
+  return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, false);
+}
+
+int attn_sync_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return attn::kStatusCuda;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return attn::kStatusCuda;
+  int value = 0;
+  const int zero = 0;
+  if (cudaMemcpyFromSymbol(&value, g_attn_status, sizeof(int)) != cudaSuccess) return attn::kStatusCuda;
+  if (value != 0 && cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int)) != cudaSuccess)
+    return attn::kStatusCuda;
+  return value;
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA runtime error";
+    case ATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case ATTN_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case ATTN_ERR_DEVICE_CHECK: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int attn_last_launch_count(void) { return attn::t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,507 @@
+// attn_bwd.cu -- recomputation backward of exact attention for sm_103a.
+//
+// Method (FlashAttention (PKM page), "三招" 3 Recomputation; FlashAttention深度攻略
+// §6): the forward keeps only O and one statistic per row (here LSE); the
+// backward rebuilds P = exp(scale Q K^T - LSE) tile by tile on chip and forms
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_k dO_ik O_ik,  dS = P o (dP - D),
+//   dK = scale dS^T Q,  dQ = scale dS K.
+//
+// Three launches on the caller's stream:
+//   1. attn_bwd_pre_kernel   : D_i (fp32), LSE * log2(e) into a padded row
+//                              vector (+inf on padding rows, so their P is 0),
+//                              and zeroes the fp32 dQ accumulator.
+//   2. attn_bwd_kernel       : one CTA per (128-key tile, head), the key tile
+//                              stays in shared memory and dK/dV accumulate in
+//                              TMEM over every query tile that can see it.
+//   3. attn_dq_convert_kernel: fp32 dQ accumulator -> bf16/fp16 dQ.
+//
+// attn_bwd_kernel roles (10 warps, one CTA per SM):
+//   * warp 8     : TMA producer: K_j and V_j once; Q_i, dO_i (2-stage ring)
+//                  plus the 128 LSE*log2e and D values of tile i (bulk copies).
+//   * warp 9     : TMEM owner and single-thread tcgen05.mma issuer, per tile i:
+//                    S^T  = K_j Q_i^T          (SS, both K-major)
+//                    dP^T = V_j dO_i^T         (SS, both K-major)
+//                    dV  += P^T dO_i           (TS, P^T from TMEM, dO MN-major)
+//                    dK  += dS^T Q_i           (SS, dS^T K-major, Q MN-major)
+//                    dQ_i = dS K_j             (SS, dS MN-major view of the same
+//                                               shared tile, K MN-major)
+//   * warps 0-3  : one thread per key row: P^T from S^T and LSE (exp2), P^T to
+//                  TMEM, dS^T = P^T o (dP^T - D) to shared memory (bf16/fp16,
+//                  128B-swizzled), and at the end the dK (x scale) / dV stores.
+//   * warps 4-7  : one thread per query row: dQ_i from TMEM, x scale, added
+//                  into the fp32 accumulator with vector reductions.
+//   * TMEM (512 columns): S^T/P^T [0,128) dP^T/dQ [128,256) dK [256,256+D)
+//                         dV [256+D,256+2D).
+// Causal: key tile j only visits query tiles i >= j; the diagonal tile is
+// masked elementwise (P^T[key][query] = 0 when key > query).
+#include "attn_internal.h"
+#include "tc_sm103.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BM = 128;  // query rows per tile
+  static constexpr int BN = 128;  // key rows per CTA
+  static constexpr int ROWB = (D >= 64) ? 128 : 64;
+  static constexpr int CH = ROWB / 2;
+  static constexpr int NCH = D / CH;
+  static constexpr uint32_t SWZ = (ROWB == 128) ? kSwizzle128B : kSwizzle64B;
+  static constexpr int SBO = 8 * ROWB;
+  static constexpr int CHUNK_BYTES = 128 * ROWB;
+  static constexpr int TILE_BYTES = 128 * D * 2;
+  static constexpr int DS_CHUNK = 128 * 128;       // 64 query columns x 128 key rows, bf16
+  static constexpr int DS_BYTES = 2 * DS_CHUNK;
+  static constexpr int NSTQ = 2;
+  static constexpr int VEC_BYTES = BM * 4;         // 128 fp32 per query tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE_BYTES;
+  static constexpr int OFF_Q = 2 * TILE_BYTES;
+  static constexpr int OFF_DO = OFF_Q + NSTQ * TILE_BYTES;
+  static constexpr int OFF_DS = OFF_DO + NSTQ * TILE_BYTES;
+  static constexpr int OFF_LSE = OFF_DS + DS_BYTES;
+  static constexpr int OFF_DD = OFF_LSE + NSTQ * VEC_BYTES;
+  static constexpr int OFF_BAR = OFF_DD + NSTQ * VEC_BYTES;
+  static constexpr int B_KVFULL = 0;
+  static constexpr int B_QFULL = 1;
+  static constexpr int B_QEMPTY = B_QFULL + NSTQ;
+  static constexpr int B_SFULL = B_QEMPTY + NSTQ;
+  static constexpr int B_DPFULL = B_SFULL + 1;
+  static constexpr int B_PFULL = B_DPFULL + 1;
+  static constexpr int B_DVDONE = B_PFULL + 1;
+  static constexpr int B_DSFULL = B_DVDONE + 1;
+  static constexpr int B_DSEMPTY = B_DSFULL + 1;
+  static constexpr int B_DQFULL = B_DSEMPTY + 1;
+  static constexpr int B_DQEMPTY = B_DQFULL + 1;
+  static constexpr int B_MMADONE = B_DQEMPTY + 1;
+  static constexpr int NBAR = B_MMADONE + 1;
+  static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
+  static constexpr int SMEM_BYTES = OFF_ABORT + 12;
+  static constexpr int THREADS = 320;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_S = 0, T_DP = 128, T_DK = 256, T_DV = 256 + D;
+  static_assert(256 + 2 * D <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+// K-major descriptor, 16-element K slice kk, of a 128-row tile with head-dim rows.
+template <int D>
+__device__ __forceinline__ uint64_t desc_k_tile(uint32_t tile, int kk) {
+  using C = BwdCfg<D>;
+  const int e = kk * 16;
+  return smem_desc(tile + (e / C::CH) * C::CHUNK_BYTES + (e % C::CH) * 2, 16, C::SBO, C::SWZ);
+}
+// MN-major descriptor (head dim contiguous), 16-row K slice kk.
+template <int D>
+__device__ __forceinline__ uint64_t desc_mn_tile(uint32_t tile, int kk) {
+  using C = BwdCfg<D>;
+  return smem_desc(tile + kk * 16 * C::ROWB, C::CHUNK_BYTES, C::SBO, C::SWZ);
+}
+// The dS^T tile: 128 key rows x 128 query columns, 128B-swizzled in two
+// 64-column chunks.  As dS^T (M = key, K = query) it is K-major ...
+__device__ __forceinline__ uint64_t desc_ds_kmajor(uint32_t tile, int kk) {
+  const int e = kk * 16;
+  return smem_desc(tile + (e / 64) * (128 * 128) + (e % 64) * 2, 16, 1024, kSwizzle128B);
+}
+// ... and as dS (M = query, K = key) it is MN-major.
+__device__ __forceinline__ uint64_t desc_ds_mnmajor(uint32_t tile, int kk) {
+  return smem_desc(tile + kk * 16 * 128, 128 * 128, 1024, kSwizzle128B);
+}
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// ------------------------------------------------------------ preprocess
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_pre_kernel(
+    const uint8_t* __restrict__ o, const uint8_t* __restrict__ dO, const float* __restrict__ lse,
+    float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc, int N, int Npad,
+    int64_t rows_total) {
+  constexpr int PER = D / 8;  // elements per lane (8 lanes per row)
+  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t rid = gid >> 3;
+  const int sub = threadIdx.x & 7;
+  const bool live = rid < rows_total;
+  const int64_t bh = live ? rid / Npad : 0;
+  const int i = live ? static_cast<int>(rid % Npad) : 0;
+  const bool real = live && i < N;
+  float acc = 0.f;
+  if (real) {
+    const int64_t off = (bh * N + i) * D + sub * PER;
+    const uint32_t* po = reinterpret_cast<const uint32_t*>(o + off * 2);
+    const uint32_t* pd = reinterpret_cast<const uint32_t*>(dO + off * 2);
+#pragma unroll
+    for (int e = 0; e < PER / 2; ++e) {
+      const float2 a = unpack2<BF16>(po[e]);
+      const float2 b = unpack2<BF16>(pd[e]);
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + off);
+#pragma unroll
+    for (int e = 0; e < PER / 4; ++e) z[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  if (live && sub == 0) {
+    dvec[rid] = real ? acc : 0.f;
+    lse2[rid] = real ? lse[bh * N + i] * kLog2e : INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------- convert
+template <bool BF16>
+__global__ void __launch_bounds__(256) attn_dq_convert_kernel(const float* __restrict__ acc,
+                                                              uint8_t* __restrict__ dq,
+                                                              int64_t groups) {
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
+       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * g];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * g + 1];
+    reinterpret_cast<uint4*>(dq)[g] = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w),
+                                                 pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
+  }
+}
+
+// -------------------------------------------------------------- main pass
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse2,
+                    const float* __restrict__ dvec, float* __restrict__ dq_acc,
+                    uint8_t* __restrict__ dk_out, uint8_t* __restrict__ dv_out, int N, int Npad,
+                    float sl2, float scale, int causal, int negate, int* status) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int jt = blockIdx.x;  // key tile (heaviest first under the causal mask)
+  const int bh = blockIdx.y;
+  const int kv0 = jt * C::BN;
+  const int ntq = (N + C::BM - 1) / C::BM;
+  const int i0 = causal ? jt : 0;
+  const int nq = ntq - i0;
+
+  const uint32_t sbase = smem_addr(smem);
+  if (sbase & 1023u) {
+    if (threadIdx.x == 0) atomicExch(status, kStatusDeviceCheck);
+    return;
+  }
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMSLOT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KVFULL), 1);
+    for (int s = 0; s < C::NSTQ; ++s) {
+      mbar_init(bar(C::B_QFULL + s), 1);
+      mbar_init(bar(C::B_QEMPTY + s), 1);
+    }
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_DPFULL), 1);
+    mbar_init(bar(C::B_PFULL), 128);
+    mbar_init(bar(C::B_DVDONE), 1);
+    mbar_init(bar(C::B_DSFULL), 128);
+    mbar_init(bar(C::B_DSEMPTY), 1);
+    mbar_init(bar(C::B_DQFULL), 1);
+    mbar_init(bar(C::B_DQEMPTY), 128);
+    mbar_init(bar(C::B_MMADONE), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_q);
+      prefetch_tensormap(&tm_k);
+      prefetch_tensormap(&tm_v);
+      prefetch_tensormap(&tm_do);
+      mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
+      for (int c = 0; c < C::NCH; ++c) {
+        tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KVFULL), c * C::CH, kv0, bh);
+        tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bar(C::B_KVFULL), c * C::CH, kv0, bh);
+      }
+      int issued = 0;
+      for (int it = 0; it < nq; ++it) {
+        const int s = it % C::NSTQ, u = it / C::NSTQ;
+        const int q0 = (i0 + it) * C::BM;
+        if (u > 0 && !mbar_wait(bar(C::B_QEMPTY + s), (u - 1) & 1, abort_flag, status)) break;
+        mbar_arrive_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE_BYTES + 2 * C::VEC_BYTES);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + s),
+                      c * C::CH, q0, bh);
+          tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar(C::B_QFULL + s),
+                      c * C::CH, q0, bh);
+        }
+        const int64_t voff = static_cast<int64_t>(bh) * Npad + q0;
+        bulk_load(sbase + C::OFF_LSE + s * C::VEC_BYTES, lse2 + voff, C::VEC_BYTES,
+                  bar(C::B_QFULL + s));
+        bulk_load(sbase + C::OFF_DD + s * C::VEC_BYTES, dvec + voff, C::VEC_BYTES,
+                  bar(C::B_QFULL + s));
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        drain_wait(bar(C::B_KVFULL), 0);
+        for (int s = 0; s < C::NSTQ; ++s) {
+          const int cnt = issued > s ? (issued - 1 - s) / C::NSTQ + 1 : 0;
+          if (cnt) drain_wait(bar(C::B_QFULL + s), (cnt - 1) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id_st = instr_desc_f16(128, 128, BF16, false, false, negate != 0);
+      const uint32_t id_dpt = instr_desc_f16(128, 128, BF16, false, false);
+      const uint32_t id_dv = instr_desc_f16(128, D, BF16, false, true);
+      const uint32_t id_dk = instr_desc_f16(128, D, BF16, false, true);
+      const uint32_t id_dq = instr_desc_f16(128, D, BF16, true, true);
+      bool ok = mbar_wait(bar(C::B_KVFULL), 0, abort_flag, status);
+      for (int it = 0; ok && it < nq; ++it) {
+        const int s = it % C::NSTQ;
+        const uint32_t ph = (it / C::NSTQ) & 1;
+        const uint32_t q_s = sQ + s * C::TILE_BYTES, do_s = sDO + s * C::TILE_BYTES;
+        if (!(ok = mbar_wait(bar(C::B_QFULL + s), ph, abort_flag, status))) break;
+        if (it > 0 && !(ok = mbar_wait(bar(C::B_DVDONE), (it - 1) & 1, abort_flag, status))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::T_S, desc_k_tile<D>(sK, kk), desc_k_tile<D>(q_s, kk), id_st,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(bar(C::B_SFULL));
+        if (it > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (it - 1) & 1, abort_flag, status))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + C::T_DP, desc_k_tile<D>(sV, kk), desc_k_tile<D>(do_s, kk), id_dpt,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(bar(C::B_DPFULL));
+        if (!(ok = mbar_wait(bar(C::B_PFULL), it & 1, abort_flag, status))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, desc_mn_tile<D>(do_s, kk), id_dv,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(C::B_DVDONE));
+        if (!(ok = mbar_wait(bar(C::B_DSFULL), it & 1, abort_flag, status))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
+                 kk > 0 ? 1u : 0u);
+        tc_commit(bar(C::B_DQFULL));
+        tc_commit(bar(C::B_QEMPTY + s));
+        tc_commit(bar(C::B_DSEMPTY));
+      }
+      tc_commit(bar(C::B_MMADONE));
+      drain_wait(bar(C::B_MMADONE), 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ----------------------------------------------- P^T and dS^T, key rows
+    const int t = threadIdx.x;  // key row within the tile, TMEM lane
+    const int kv_row = kv0 + t;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float* sLSE = reinterpret_cast<const float*>(smem + C::OFF_LSE);
+    const float* sDD = reinterpret_cast<const float*>(smem + C::OFF_DD);
+    uint8_t* ds_tile = smem + C::OFF_DS;
+    bool ok = true;
+    for (int it = 0; it < nq; ++it) {
+      const int s = it % C::NSTQ;
+      const int q0 = (i0 + it) * C::BM;
+      if (!(ok = mbar_wait(bar(C::B_SFULL), it & 1, abort_flag, status))) break;
+      tc_fence_after_sync();
+      float p[128];
+      {
+        uint32_t u[64];
+        tmem_ld64(tmem + lane_off + C::T_S, u);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
+        tmem_ld64(tmem + lane_off + C::T_S + 64, u);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[64 + c] = __uint_as_float(u[c]);
+      }
+      const float* lse_s = sLSE + s * C::BM;
+      // query q0 + c sees this key iff kv_row <= q0 + c (causal); key rows >= N are padding
+      int first = 0;
+      if (kv_row >= N) first = 128;
+      else if (causal && kv_row > q0) first = min(kv_row - q0, 128);
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float e = ex2_approx(fmaf(p[c], sl2, -lse_s[c]));
+        p[c] = (c >= first) ? e : 0.f;
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < 2; ++c0) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[c0 * 64 + 2 * i], p[c0 * 64 + 2 * i + 1]);
+        tmem_st32(tmem + lane_off + C::T_S + c0 * 32, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::B_PFULL));
+
+      if (!(ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status))) break;
+      if (it > 0 && !(ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status))) break;
+      tc_fence_after_sync();
+      const float* dd_s = sDD + s * C::BM;
+#pragma unroll
+      for (int c0 = 0; c0 < 4; ++c0) {
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 * 32 + 2 * i;
+          const float a = p[c] * (__uint_as_float(dp[2 * i]) - dd_s[c]);
+          const float b = p[c + 1] * (__uint_as_float(dp[2 * i + 1]) - dd_s[c + 1]);
+          pk[i] = pack2<BF16>(a, b);
+        }
+        // query columns [c0*32, c0*32+32): chunk c0/2, 16-byte units (c0%2)*4 .. +3
+        uint8_t* rowp = ds_tile + (c0 >> 1) * C::DS_CHUNK + t * 128;
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+          const int unit = ((c0 & 1) * 4 + uu) ^ (t & 7);
+          *reinterpret_cast<uint4*>(rowp + unit * 16) =
+              make_uint4(pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::B_DSFULL));
+    }
+    // dK, dV epilogue once the last dK/dQ MMAs have completed
+    if (ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status)) {
+      tc_fence_after_sync();
+      const int64_t rbase = (static_cast<int64_t>(bh) * N + kv_row) * (D * 2);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tcol = tmem + lane_off + (which == 0 ? C::T_DK : C::T_DV);
+        const float mul = which == 0 ? scale : 1.f;
+        uint8_t* dst_row = (which == 0 ? dk_out : dv_out) + rbase;
+#pragma unroll
+        for (int c0 = 0; c0 < D / 32; ++c0) {
+          uint32_t v[32];
+          tmem_ld32(tcol + c0 * 32, v);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+          if (kv_row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 64);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ dQ, query rows (warps 4-7)
+    const int t = threadIdx.x - 128;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int it = 0; it < nq; ++it) {
+      const int qrow = (i0 + it) * C::BM + t;
+      if (!mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status)) break;
+      tc_fence_after_sync();
+      float dq[D];
+#pragma unroll
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dq[c0 * 32 + i] = __uint_as_float(v[i]) * scale;
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::B_DQEMPTY));
+      if (qrow < N) {
+        float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 4) red_add_v4(dst + c, dq[c], dq[c + 1], dq[c + 2], dq[c + 3]);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool BF16>
+int launch_bwd_t(const BwdArgs& a) {
+  using C = BwdCfg<D>;
+  const int Npad = ((a.N + 127) / 128) * 128;
+  const int64_t rows_total = static_cast<int64_t>(a.BH) * Npad;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_bhnd_map(&mq, a.q, a.BH, a.N, D, C::CH, 128, C::ROWB, BF16) ||
+      !encode_bhnd_map(&mk, a.k, a.BH, a.N, D, C::CH, 128, C::ROWB, BF16) ||
+      !encode_bhnd_map(&mv, a.v, a.BH, a.N, D, C::CH, 128, C::ROWB, BF16) ||
+      !encode_bhnd_map(&mdo, a.dO, a.BH, a.N, D, C::CH, 128, C::ROWB, BF16))
+    return kStatusCuda;
+  auto kern = attn_bwd_kernel<D, BF16>;
+  if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
+  {
+    const int64_t threads = rows_total * 8;
+    const int blocks = static_cast<int>((threads + 255) / 256);
+    attn_bwd_pre_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(
+        static_cast<const uint8_t*>(a.o), static_cast<const uint8_t*>(a.dO), a.lse, a.ws_lse2,
+        a.ws_d, a.ws_dq, a.N, Npad, rows_total);
+  }
+  dim3 grid((a.N + C::BN - 1) / C::BN, a.BH);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(
+      mq, mk, mv, mdo, a.ws_lse2, a.ws_d, a.ws_dq, static_cast<uint8_t*>(a.dk),
+      static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status);
+  {
+    const int64_t groups = static_cast<int64_t>(a.BH) * a.N * D / 8;
+    const int blocks = static_cast<int>(std::min<int64_t>((groups + 255) / 256, 152 * 16));
+    attn_dq_convert_kernel<BF16><<<blocks, 256, 0, a.stream>>>(a.ws_dq,
+                                                               static_cast<uint8_t*>(a.dq), groups);
+  }
+  return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
+}
+
+}  // namespace
+
+int launch_bwd(const BwdArgs& a) {
+  switch (a.d) {
+    case 32: return a.bf16 ? launch_bwd_t<32, true>(a) : launch_bwd_t<32, false>(a);
+    case 64: return a.bf16 ? launch_bwd_t<64, true>(a) : launch_bwd_t<64, false>(a);
+    case 128: return a.bf16 ? launch_bwd_t<128, true>(a) : launch_bwd_t<128, false>(a);
+    default: return kStatusUnsupported;
+  }
+}
+
+}  // namespace attn

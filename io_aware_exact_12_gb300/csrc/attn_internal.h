@@ -1,0 +1,70 @@
+// attn_internal.h -- declarations shared by the library's translation units
+// (host launchers, argument bundles, status codes).  Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+namespace attn {
+
+// Status codes; the public values are those of attn_status_t in attn.h.
+constexpr int kStatusOk = 0;
+constexpr int kStatusInvalid = 1;
+constexpr int kStatusUnsupported = 2;
+constexpr int kStatusCuda = 3;
+constexpr int kStatusTimeout = 4;
+constexpr int kStatusArch = 5;
+constexpr int kStatusDeviceCheck = 6;
+
+struct FwdArgs {
+  const void *q, *k, *v;
+  void* o;
+  float* lse;
+  int BH, N, d;
+  float sl2;  // |scale| * log2(e)
+  int causal;
+  int negate;  // scale < 0: the S MMA negates its A operand
+  bool bf16;
+  cudaStream_t stream;
+  int* status;
+};
+
+struct BwdArgs {
+  const void *q, *k, *v, *o, *dO;
+  const float* lse;
+  void *dq, *dk, *dv;
+  int BH, N, d;
+  float sl2;    // |scale| * log2(e)
+  float scale;  // signed, applied to dQ and dK
+  int causal;
+  int negate;
+  bool bf16;
+  cudaStream_t stream;
+  int* status;
+  // scratch (device): fp32 dQ accumulator [BH][N][d]; LSE*log2e and D, [BH][Npad]
+  float* ws_dq;
+  float* ws_lse2;
+  float* ws_d;
+};
+
+// Bytes of backward scratch for a problem, and its carve-up.
+struct BwdScratch {
+  size_t dq_off, lse2_off, d_off, total;
+};
+BwdScratch bwd_scratch_layout(int BH, int N, int d);
+
+// 3-D tiled tensor map over a [BH][N][d] tensor: dims (d, N, BH), box
+// (box_inner, box_rows, 1), 128- or 64-byte swizzle by row_bytes, zero fill.
+bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_inner,
+                     int box_rows, int row_bytes, bool bf16);
+
+// Raises the kernel's dynamic shared-memory limit once per device.
+bool ensure_smem_attr(const void* func, int bytes);
+
+int launch_fwd(const FwdArgs& a);
+int launch_bwd(const BwdArgs& a);
+
+}  // namespace attn

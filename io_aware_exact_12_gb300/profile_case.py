@@ -1,0 +1,62 @@
+"""Runs one attention op a fixed number of times on synthetic inputs, for
+capturing it under a profiler (ncu).  Warm-up launches come first, so a
+capture can skip them with ``-s``.
+
+  python -m io_aware_exact_12_gb300.profile_case --op fwd --B 2 --H 16 --N 8192 --d 128 --launches 2
+  python -m io_aware_exact_12_gb300.profile_case --op bwd ...   (one attn_bwd = 3 launches)
+  python -m io_aware_exact_12_gb300.profile_case --op naive ... (materialising 3-step
+      torch comparator: S = QK^T, P = softmax(S), O = PV, to measure its DRAM bytes)
+"""
+from __future__ import annotations
+
+import argparse
+import math
+
+import torch
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--op", choices=["fwd", "bwd", "naive"], default="fwd")
+    ap.add_argument("--B", type=int, default=2)
+    ap.add_argument("--H", type=int, default=16)
+    ap.add_argument("--N", type=int, default=8192)
+    ap.add_argument("--d", type=int, default=128)
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--dtype", default="bf16")
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--launches", type=int, default=2)
+    a = ap.parse_args(argv)
+
+    import io_aware_exact_12_gb300 as attn
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+    x = make_inputs(AttnShape(a.B, a.H, a.N, a.d), a.dtype, seed=4, device="cuda")
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    scale = 1.0 / math.sqrt(a.d)
+    o, lse = attn.attn_fwd(q, k, v, scale=scale, causal=a.causal)
+
+    def run():
+        if a.op == "fwd":
+            attn.attn_fwd(q, k, v, scale=scale, causal=a.causal, o=o, lse=lse)
+        elif a.op == "bwd":
+            attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=a.causal)
+        else:
+            s = torch.matmul(q, k.transpose(-2, -1)) * scale
+            if a.causal:
+                s = s.masked_fill(torch.ones(a.N, a.N, dtype=torch.bool, device=q.device).triu(1),
+                                  float("-inf"))
+            torch.matmul(torch.softmax(s, dim=-1), v)
+
+    for _ in range(a.warmup):
+        run()
+    torch.cuda.synchronize()
+    for _ in range(a.launches):
+        run()
+    torch.cuda.synchronize()
+    st = attn.sync_status()
+    print("done op=%s status=%d" % (a.op, st))
+    return 1 if st else 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
