@@ -126,6 +126,12 @@ bool ensure_smem_attr(const void* func, int bytes) {
   return true;
 }
 
+bool check_launch_regs(const void* func, int regs) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) return false;
+  return fa.numRegs == regs;
+}
+
 BwdScratch bwd_scratch_layout(int BH, int N, int d) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t Npad = static_cast<size_t>((N + 127) / 128) * 128;

@@ -7,29 +7,34 @@
 //   dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three launches on the caller's stream:
-//   1. attn_bwd_pre_kernel   : D_i (fp32), LSE * log2(e) into a padded row
-//                              vector (+inf on padding rows, so their P is 0),
+//   1. attn_bwd_pre_kernel   : -D_i (fp32) and -LSE * log2(e) into padded row
+//                              vectors (-inf on padding rows, so their P is 0),
 //                              and zeroes the fp32 dQ accumulator.
 //   2. attn_bwd_kernel       : one CTA per (128-key tile, head), the key tile
 //                              stays in shared memory and dK/dV accumulate in
 //                              TMEM over every query tile that can see it.
 //   3. attn_dq_convert_kernel: fp32 dQ accumulator -> bf16/fp16 dQ.
 //
-// attn_bwd_kernel roles (10 warps, one CTA per SM):
-//   * warp 8     : TMA producer: K_j and V_j once; Q_i, dO_i (2-stage ring)
-//                  plus the 128 LSE*log2e and D values of tile i (bulk copies).
-//   * warp 9     : TMEM owner and single-thread tcgen05.mma issuer, per tile i:
+// attn_bwd_kernel roles (16 warps = 4 warpgroups, one CTA per SM; warpgroup 3
+// hands registers to warpgroups 0 and 1 with setmaxnreg, 80 / 152):
+//   * warp 12    : TMA producer: K_j and V_j once; Q_i, dO_i (2-stage ring)
+//                  plus the 128 -LSE*log2e and -D values of tile i (bulk copies).
+//   * warp 13    : TMEM owner and single-thread tcgen05.mma issuer, per tile i:
 //                    S^T  = K_j Q_i^T          (SS, both K-major)
 //                    dP^T = V_j dO_i^T         (SS, both K-major)
 //                    dV  += P^T dO_i           (TS, P^T from TMEM, dO MN-major)
 //                    dK  += dS^T Q_i           (SS, dS^T K-major, Q MN-major)
 //                    dQ_i = dS K_j             (SS, dS MN-major view of the same
 //                                               shared tile, K MN-major)
-//   * warps 0-3  : one thread per key row: P^T from S^T and LSE (exp2), P^T to
-//                  TMEM, dS^T = P^T o (dP^T - D) to shared memory (bf16/fp16,
-//                  128B-swizzled), and at the end the dK (x scale) / dV stores.
-//   * warps 4-7  : one thread per query row: dQ_i from TMEM, x scale, added
-//                  into the fp32 accumulator with vector reductions.
+//   * warps 0-7  : two threads per key row (warpgroup g takes query columns
+//                  64g..64g+63): P^T from S^T and LSE (exp2), P^T to TMEM,
+//                  dS^T = P^T o (dP^T - D) to shared memory (bf16/fp16,
+//                  128B-swizzled); at the end warpgroup 0 stores dK (x scale)
+//                  and warpgroup 1 stores dV.
+//   * warps 8-11 : one thread per query row: dQ_i from TMEM in 32-column
+//                  chunks, x scale, added into the fp32 accumulator with
+//                  vector reductions.
+//   * warps 14-15: idle (they complete warpgroup 3 for the register split).
 //   * TMEM (512 columns): S^T/P^T [0,128) dP^T/dQ [128,256) dK [256,256+D)
 //                         dV [256+D,256+2D).
 // Causal: key tile j only visits query tiles i >= j; the diagonal tile is
@@ -82,7 +87,12 @@ struct BwdCfg {
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 12;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 512;
+  static constexpr int REGS_LAUNCH = 128;
+  static constexpr int REGS_MATH = 152;  // the two P / dS warpgroups
+  static constexpr int REGS_CTRL = 80;   // producer / MMA warpgroup
+  static_assert(128 * (2 * REGS_MATH + REGS_LAUNCH + REGS_CTRL) <= THREADS * REGS_LAUNCH,
+                "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DK = 256, T_DV = 256 + D;
   static_assert(256 + 2 * D <= 512, "TMEM budget");
@@ -126,6 +136,7 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(
     const uint8_t* __restrict__ o, const uint8_t* __restrict__ dO, const float* __restrict__ lse,
     float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc, int N, int Npad,
     int64_t rows_total) {
+  // lse2 receives -LSE * log2(e) and dvec receives -D, the forms the main pass adds.
   constexpr int PER = D / 8;  // elements per lane (8 lanes per row)
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t rid = gid >> 3;
@@ -154,8 +165,8 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   if (live && sub == 0) {
-    dvec[rid] = real ? acc : 0.f;
-    lse2[rid] = real ? lse[bh * N + i] * kLog2e : INFINITY;
+    dvec[rid] = real ? -acc : 0.f;
+    lse2[rid] = real ? -lse[bh * N + i] * kLog2e : -INFINITY;
   }
 }
 
@@ -212,9 +223,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
-    mbar_init(bar(C::B_PFULL), 128);
+    mbar_init(bar(C::B_PFULL), 256);
     mbar_init(bar(C::B_DVDONE), 1);
-    mbar_init(bar(C::B_DSFULL), 128);
+    mbar_init(bar(C::B_DSFULL), 256);
     mbar_init(bar(C::B_DSEMPTY), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQEMPTY), 128);
@@ -222,7 +233,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -234,9 +245,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
   const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp >= 12) {
+    regs_decrease<C::REGS_CTRL>();
+    if (warp == 12 && lane == 0) {
+      // ---------------------------------------------------------- producer
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
@@ -272,11 +284,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           if (cnt) drain_wait(bar(C::B_QFULL + s), (cnt - 1) & 1);
         }
       }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    } else if (warp == 13 && lane == 0) {
+      // -------------------------------------------------------- MMA issuer
       const uint32_t id_st = instr_desc_f16(128, 128, BF16, false, false, negate != 0);
       const uint32_t id_dpt = instr_desc_f16(128, 128, BF16, false, false);
       const uint32_t id_dv = instr_desc_f16(128, D, BF16, false, true);
@@ -306,8 +315,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + kk * 8, desc_mn_tile<D>(do_s, kk), id_dv,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                 desc_mn_tile<D>(do_s, kk), id_dv, (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(bar(C::B_DVDONE));
         if (!(ok = mbar_wait(bar(C::B_DSFULL), it & 1, abort_flag, status))) break;
         tc_fence_after_sync();
@@ -327,46 +336,51 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       drain_wait(bar(C::B_MMADONE), 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ----------------------------------------------- P^T and dS^T, key rows
-    const int t = threadIdx.x;  // key row within the tile, TMEM lane
+  } else if (warp < 8) {
+    // ------------------------------------- P^T and dS^T, key rows, half a row each
+    regs_increase<C::REGS_MATH>();
+    const int g = warp >> 2;            // query columns 64g .. 64g+63
+    const int t = threadIdx.x & 127;    // key row within the tile, TMEM lane
     const int kv_row = kv0 + t;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float* sLSE = reinterpret_cast<const float*>(smem + C::OFF_LSE);
     const float* sDD = reinterpret_cast<const float*>(smem + C::OFF_DD);
-    uint8_t* ds_tile = smem + C::OFF_DS;
+    uint8_t* ds_row = smem + C::OFF_DS + g * C::DS_CHUNK + t * 128;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
     for (int it = 0; it < nq; ++it) {
       const int s = it % C::NSTQ;
-      const int q0 = (i0 + it) * C::BM;
+      const int q0 = (i0 + it) * C::BM + g * 64;  // first query of this thread's half
       if (!(ok = mbar_wait(bar(C::B_SFULL), it & 1, abort_flag, status))) break;
       tc_fence_after_sync();
-      float p[128];
+      float p[64];
       {
         uint32_t u[64];
-        tmem_ld64(tmem + lane_off + C::T_S, u);
+        tmem_ld64(tmem + lane_off + C::T_S + g * 64, u);
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = __uint_as_float(u[c]);
-        tmem_ld64(tmem + lane_off + C::T_S + 64, u);
-#pragma unroll
-        for (int c = 0; c < 64; ++c) p[64 + c] = __uint_as_float(u[c]);
       }
-      const float* lse_s = sLSE + s * C::BM;
+      const float2* nlse = reinterpret_cast<const float2*>(sLSE + s * C::BM + g * 64);  // -LSE*log2(e)
       // query q0 + c sees this key iff kv_row <= q0 + c (causal); key rows >= N are padding
       int first = 0;
-      if (kv_row >= N) first = 128;
-      else if (causal && kv_row > q0) first = min(kv_row - q0, 128);
+      if (kv_row >= N) first = 64;
+      else if (causal && kv_row > q0) first = min(kv_row - q0, 64);
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float e = ex2_approx(fmaf(p[c], sl2, -lse_s[c]));
-        p[c] = (c >= first) ? e : 0.f;
+      for (int c = 0; c < 64; c += 2) {
+        const float2 e = fma2(make_float2(p[c], p[c + 1]), sl2x2, nlse[c / 2]);
+        p[c] = ex2_approx(e.x);
+        p[c + 1] = ex2_approx(e.y);
       }
+      if (first > 0) {
 #pragma unroll
-      for (int c0 = 0; c0 < 2; ++c0) {
+        for (int c = 0; c < 64; ++c)
+          if (c < first) p[c] = 0.f;
+      }
+      {
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[c0 * 64 + 2 * i], p[c0 * 64 + 2 * i + 1]);
-        tmem_st32(tmem + lane_off + C::T_S + c0 * 32, pk);
+        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+        tmem_st32(tmem + lane_off + C::T_S + g * 64, pk);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -375,25 +389,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       if (!(ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status))) break;
       if (it > 0 && !(ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status))) break;
       tc_fence_after_sync();
-      const float* dd_s = sDD + s * C::BM;
+      const float2* nd = reinterpret_cast<const float2*>(sDD + s * C::BM + g * 64);  // -D
 #pragma unroll
-      for (int c0 = 0; c0 < 4; ++c0) {
+      for (int c0 = 0; c0 < 2; ++c0) {
         uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, dp);
+        tmem_ld32(tmem + lane_off + C::T_DP + g * 64 + c0 * 32, dp);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = c0 * 32 + 2 * i;
-          const float a = p[c] * (__uint_as_float(dp[2 * i]) - dd_s[c]);
-          const float b = p[c + 1] * (__uint_as_float(dp[2 * i + 1]) - dd_s[c + 1]);
-          pk[i] = pack2<BF16>(a, b);
+          const float2 gd = add2(make_float2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])),
+                                 nd[c / 2]);
+          const float2 ds = mul2(make_float2(p[c], p[c + 1]), gd);
+          pk[i] = pack2<BF16>(ds.x, ds.y);
         }
-        // query columns [c0*32, c0*32+32): chunk c0/2, 16-byte units (c0%2)*4 .. +3
-        uint8_t* rowp = ds_tile + (c0 >> 1) * C::DS_CHUNK + t * 128;
+        // this chunk's 32 query columns are 16-byte units c0*4 .. c0*4+3 of the row
 #pragma unroll
         for (int uu = 0; uu < 4; ++uu) {
-          const int unit = ((c0 & 1) * 4 + uu) ^ (t & 7);
-          *reinterpret_cast<uint4*>(rowp + unit * 16) =
+          const int unit = (c0 * 4 + uu) ^ (t & 7);
+          *reinterpret_cast<uint4*>(ds_row + unit * 16) =
               make_uint4(pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
         }
       }
@@ -401,60 +415,56 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_DSFULL));
     }
-    // dK, dV epilogue once the last dK/dQ MMAs have completed
+    // dK (warpgroup 0) or dV (warpgroup 1) once the last MMAs have completed
     if (ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status)) {
       tc_fence_after_sync();
       const int64_t rbase = (static_cast<int64_t>(bh) * N + kv_row) * (D * 2);
+      const uint32_t tcol = tmem + lane_off + (g == 0 ? C::T_DK : C::T_DV);
+      const float mul = g == 0 ? scale : 1.f;
+      uint8_t* dst_row = (g == 0 ? dk_out : dv_out) + rbase;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t tcol = tmem + lane_off + (which == 0 ? C::T_DK : C::T_DV);
-        const float mul = which == 0 ? scale : 1.f;
-        uint8_t* dst_row = (which == 0 ? dk_out : dv_out) + rbase;
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t v[32];
+        tmem_ld32(tcol + c0 * 32, v);
+        uint32_t pk[16];
 #pragma unroll
-        for (int c0 = 0; c0 < D / 32; ++c0) {
-          uint32_t v[32];
-          tmem_ld32(tcol + c0 * 32, v);
-          uint32_t pk[16];
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+        if (kv_row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 64);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-          if (kv_row < N) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 64);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
     }
   } else {
-    // ------------------------------------------------ dQ, query rows (warps 4-7)
-    const int t = threadIdx.x - 128;
+    // ----------------------------------------------- dQ, query rows (warps 8-11)
+    const int t = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int it = 0; it < nq; ++it) {
       const int qrow = (i0 + it) * C::BM + t;
       if (!mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status)) break;
       tc_fence_after_sync();
-      float dq[D];
+      float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, v);
+        if (qrow < N) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dq[c0 * 32 + i] = __uint_as_float(v[i]) * scale;
+          for (int c = 0; c < 32; c += 4)
+            red_add_v4(dst + c0 * 32 + c, __uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
+                       __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
+        }
       }
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_DQEMPTY));
-      if (qrow < N) {
-        float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
-#pragma unroll
-        for (int c = 0; c < D; c += 4) red_add_v4(dst + c, dq[c], dq[c + 1], dq[c + 2], dq[c + 3]);
-      }
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
@@ -473,6 +483,7 @@ int launch_bwd_t(const BwdArgs& a) {
     return kStatusCuda;
   auto kern = attn_bwd_kernel<D, BF16>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
+  if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   {
     const int64_t threads = rows_total * 8;
     const int blocks = static_cast<int>((threads + 255) / 256);

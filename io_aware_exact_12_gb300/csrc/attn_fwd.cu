@@ -7,10 +7,12 @@
 // O and l by exp(m_old - m_new) whenever the max grows, and divide by l once
 // at the end.  S = Q K^T and P never leave the SM.
 //
-// GB300 mapping (one CTA per SM, 10 warps):
+// GB300 mapping (one CTA per SM, 12 warps = 3 warpgroups):
 //   * CTA = 256 query rows of one (batch, head): two 128-row tiles Q0, Q1 that
 //     take turns on the tensor core (while one tile's softmax runs, the other
 //     tile's MMAs do), sharing every K/V tile loaded.
+//   * warpgroup 2 (warps 8-11) gives most of its registers to the two
+//     softmax warpgroups (setmaxnreg 56 / 224), then:
 //   * warp 8  : TMA producer -- Q0/Q1 once, then K_j and V_j into an
 //               NST-stage ring (128B-swizzled tiles, 3-D tensor maps so a
 //               tile never straddles two heads and rows >= N read as zero).
@@ -18,11 +20,15 @@
 //               S_q = Q_q K_j^T  (SS: both operands K-major in shared memory)
 //               O_q += P_q V_j   (TS: P from TMEM, V MN-major in shared memory)
 //   * warps 0-3 / 4-7 : softmax for Q0 / Q1, one thread per query row (TMEM
-//               lane).  exp2 with scale*log2(e) folded in; the reference max is
+//               lane), 224 registers each so a whole 128-wide row of S stays in
+//               registers.  exp2 with scale*log2(e) folded in (packed f32x2
+//               FMAs, three-input max, split accumulators); the reference max is
 //               only moved when it grows by more than 2^8 (the same stale max
 //               is used for l and for P, so the result is unchanged); O is
 //               rescaled in TMEM by the same thread; P is written back to TMEM
-//               as bf16/fp16 over the first half of its S columns.
+//               as bf16/fp16 over the first half of its S columns.  l is kept
+//               twice: the exact sum for LSE, and the sum of the rounded P
+//               values (the weights actually applied to V) to normalise O.
 //   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied; only the diagonal tile (and the ragged last tile) are masked.
@@ -66,7 +72,11 @@ struct FwdCfg {
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 12;
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 384;
+  static constexpr int REGS_LAUNCH = 168;   // 65536 / 384, rounded down to a multiple of 8
+  static constexpr int REGS_MATH = 224;     // softmax warpgroups
+  static constexpr int REGS_CTRL = 56;      // producer / MMA warpgroup
+  static_assert(2 * 128 * REGS_MATH + 128 * REGS_CTRL <= THREADS * REGS_LAUNCH, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(2 * 128 + 2 * D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -159,9 +169,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    regs_decrease<C::REGS_CTRL>();
+    if (warp == 8 && lane == 0) {
+      // ---------------------------------------------------------- producer
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
@@ -200,50 +211,80 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           if (cv) drain_wait(bar(C::B_VFULL + s), (cv - 1) & 1);
         }
       }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    } else if (warp == 9 && lane == 0) {
+      // -------------------------------------------------------- MMA issuer
+      // Each query tile runs its own chain S(0), PV(0), S(1), PV(1), ...; the
+      // issuer polls both chains and issues whichever next MMA group is ready,
+      // so one tile's softmax never holds up the other tile's MMAs.
+      //   S_q(j)  needs K_j resident and PV_q(j-1) complete (P_q aliases S_q);
+      //   PV_q(j) needs V_j resident and P_q(j) written by the softmax.
+      // A K (V) stage is released once both tiles have issued their S (PV) on it.
       const uint32_t idesc_s = instr_desc_f16(C::BM, C::BN, BF16, false, false, negate != 0);
       const uint32_t idesc_o = instr_desc_f16(C::BM, D, BF16, false, true);
       bool ok = nkv_max == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
-      for (int j = 0; ok && j < nkv_max; ++j) {
-        const int s = j % C::NST;
-        const uint32_t ph = (j / C::NST) & 1;
-        if (!(ok = mbar_wait(bar(C::B_KFULL + s), ph, abort_flag, status))) break;
-        tc_fence_after_sync();
-        for (int q = 0; q < 2 && ok; ++q) {
-          if (j >= nkv[q]) continue;
-          if (j > 0) {  // P_q of the previous step must be consumed before S_q is overwritten
-            if (!(ok = mbar_wait(bar(C::B_ODONE + q), (j - 1) & 1, abort_flag, status))) break;
+      tc_fence_after_sync();
+      int js[2] = {0, 0};  // next S index per tile
+      int jp[2] = {0, 0};  // next PV index per tile
+      int k_rel = 0, v_rel = 0;  // next key/value tile whose stage is still held
+      uint64_t t_idle = global_timer_ns();
+      while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
+        bool progress = false;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          // PV_q(jp)
+          const int jv = jp[q];
+          if (jv < nkv[q] && jv < js[q] &&
+              mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
+              mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
             tc_fence_after_sync();
+            const uint32_t d_o = tmem + 2 * C::BN + q * D;
+            const uint32_t a_p = tmem + q * C::BN;
+            const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 16; ++kk)
+              mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar(C::B_ODONE + q));
+            jp[q] = jv + 1;
+            progress = true;
           }
-          const uint32_t d_s = tmem + q * C::BN;
+          // S_q(js)
+          const int jk = js[q];
+          if (jk < nkv[q] && jk == jp[q] &&
+              mbar_probe(bar(C::B_KFULL + jk % C::NST), (jk / C::NST) & 1) &&
+              (jk == 0 || mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1))) {
+            tc_fence_after_sync();
+            const uint32_t d_s = tmem + q * C::BN;
+            const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk),
-                   desc_kmajor<D>(sK + s * C::TILE_BYTES, kk), idesc_s, kk > 0 ? 1u : 0u);
-          tc_commit(bar(C::B_SFULL + q));
+            for (int kk = 0; kk < D / 16; ++kk)
+              mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
+                     kk > 0 ? 1u : 0u);
+            tc_commit(bar(C::B_SFULL + q));
+            js[q] = jk + 1;
+            progress = true;
+          }
         }
-        if (!ok) break;
-        tc_commit(bar(C::B_KEMPTY + s));
-        if (!(ok = mbar_wait(bar(C::B_VFULL + s), ph, abort_flag, status))) break;
-        tc_fence_after_sync();
-        for (int q = 0; q < 2 && ok; ++q) {
-          if (j >= nkv[q]) continue;
-          if (!(ok = mbar_wait(bar(C::B_PFULL + q), j & 1, abort_flag, status))) break;
-          tc_fence_after_sync();
-          const uint32_t d_o = tmem + 2 * C::BN + q * D;
-          const uint32_t a_p = tmem + q * C::BN;
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(sV + s * C::TILE_BYTES, kk), idesc_o,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(C::B_ODONE + q));
+        // release stages both tiles are done issuing from
+        while (k_rel < nkv_max && (js[0] > k_rel || k_rel >= nkv[0]) && (js[1] > k_rel || k_rel >= nkv[1])) {
+          tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
+          ++k_rel;
         }
-        if (!ok) break;
-        tc_commit(bar(C::B_VEMPTY + s));
+        while (v_rel < nkv_max && (jp[0] > v_rel || v_rel >= nkv[0]) && (jp[1] > v_rel || v_rel >= nkv[1])) {
+          tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
+          ++v_rel;
+        }
+        if (progress) {
+          t_idle = global_timer_ns();
+        } else {
+          if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
+            *abort_flag = 1;
+            ok = false;
+          } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicExch(status, kStatusTimeout);
+            ok = false;
+          }
+        }
       }
       // Every MMA issued above must finish before TMEM is released.
       tc_commit(bar(C::B_MMADONE));
@@ -252,6 +293,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
+    regs_increase<C::REGS_MATH>();
     const int q = warp >> 2;
     const int r = threadIdx.x & 127;
     const int row0 = qb * 2 * C::BM + q * C::BM;
@@ -259,9 +301,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + q * C::BN;
     const uint32_t tO = tmem + lane_off + 2 * C::BN + q * D;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;   // reference max (log2 units), moved lazily
+    float l_exact = 0.f;   // sum of exp2(t - m) in fp32: gives LSE
+    float l_round = 0.f;   // sum of the rounded P values: normalises O
     bool ok = true;
     const int nk = nkv[q];
+    const float2 sl2x2 = make_float2(sl2, sl2);
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
       tc_fence_after_sync();
@@ -285,9 +330,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) sv[c] = -INFINITY;
       }
-      float mx = sv[0];
+      float mx;
+      {
+        float a0 = sv[0], a1 = sv[1], a2 = sv[2], a3 = sv[3];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        for (int c = 4; c < 128; c += 8) {
+          a0 = max3f(a0, sv[c], sv[c + 1]);
+          a1 = max3f(a1, sv[c + 2], sv[c + 3]);
+          a2 = max3f(a2, sv[c + 4], sv[c + 5]);
+          a3 = max3f(a3, sv[c + 6], sv[c + 7]);
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      }
       const float m_new = fmaxf(m, mx * sl2);
       float alpha = 1.f;
       if (m_new > m + kRescaleThresholdLog2) {  // also taken on the first tile (m = -inf)
@@ -295,12 +349,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         m = m_new;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float2 t = fma2(make_float2(sv[c], sv[c + 1]), sl2x2, nm2);
+        sv[c] = ex2_approx(t.x);
+        sv[c + 1] = ex2_approx(t.y);
+      }
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) sv[c] = (c < lim) ? ex2_approx(fmaf(sv[c], sl2, neg_m)) : 0.f;
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) sv[c] = ex2_approx(fmaf(sv[c], sl2, neg_m));
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) sv[c] = 0.f;
       }
       // O_q holds the previous steps' sum: rescale it when any row of this warp moved its max.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -313,21 +372,26 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           tmem_st32(tO + c0 * 32, ov);
         }
       }
-      // P is rounded to the input type for the P V product; l sums the rounded
-      // values, so the weights that multiply V sum to exactly l.
-      float rs = 0.f;
+      // P is rounded to the input type for the P V product.
+      float2 se0 = make_float2(0.f, 0.f), se1 = se0, sr0 = se0, sr1 = se0;
 #pragma unroll
       for (int c0 = 0; c0 < 2; ++c0) {
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          pk[i] = pack2<BF16>(sv[c0 * 64 + 2 * i], sv[c0 * 64 + 2 * i + 1]);
-          const float2 r = unpack2<BF16>(pk[i]);
-          rs += r.x + r.y;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 p0 = make_float2(sv[c0 * 64 + 2 * i], sv[c0 * 64 + 2 * i + 1]);
+          const float2 p1 = make_float2(sv[c0 * 64 + 2 * i + 2], sv[c0 * 64 + 2 * i + 3]);
+          pk[i] = pack2<BF16>(p0.x, p0.y);
+          pk[i + 1] = pack2<BF16>(p1.x, p1.y);
+          se0 = add2(se0, p0);
+          se1 = add2(se1, p1);
+          sr0 = add2(sr0, unpack2<BF16>(pk[i]));
+          sr1 = add2(sr1, unpack2<BF16>(pk[i + 1]));
         }
         tmem_st32(tS + c0 * 32, pk);
       }
-      l = l * alpha + rs;
+      l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
+      l_round = l_round * alpha + ((sr0.x + sr0.y) + (sr1.x + sr1.y));
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL + q));
@@ -335,7 +399,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && nk > 0 && mbar_wait(bar(C::B_ODONE + q), (nk - 1) & 1, abort_flag, status)) {
       tc_fence_after_sync();
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / l_round;
       uint8_t* orow = o_out + (static_cast<int64_t>(bh) * N + row) * (D * 2);
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -351,7 +415,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (row < N) lse_out[static_cast<int64_t>(bh) * N + row] = (m + log2f(l)) * 0.69314718055994531f;
+      if (row < N) lse_out[static_cast<int64_t>(bh) * N + row] = (m + log2f(l_exact)) * 0.69314718055994531f;
     }
   }
 
@@ -374,6 +438,8 @@ int launch_fwd_t(const FwdArgs& a) {
     return kStatusCuda;
   auto kern = attn_fwd_kernel<D, BF16>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
+  // The warpgroup register split adds up only at this launch allocation.
+  if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, static_cast<uint8_t*>(a.o), a.lse,
                                                       a.N, a.sl2, a.causal, a.negate, a.status);

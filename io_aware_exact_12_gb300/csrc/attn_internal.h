@@ -64,6 +64,10 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, i
 // Raises the kernel's dynamic shared-memory limit once per device.
 bool ensure_smem_attr(const void* func, int bytes);
 
+// True iff the kernel was built with exactly `regs` registers per thread (a
+// warpgroup register split that does not add up would wait forever).
+bool check_launch_regs(const void* func, int regs);
+
 int launch_fwd(const FwdArgs& a);
 int launch_bwd(const BwdArgs& a);
 
