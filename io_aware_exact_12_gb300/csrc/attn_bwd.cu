@@ -16,7 +16,7 @@
 //   3. attn_dq_convert_kernel: fp32 dQ accumulator -> bf16/fp16 dQ.
 //
 // attn_bwd_kernel roles (16 warps = 4 warpgroups, one CTA per SM; warpgroup 3
-// hands registers to warpgroups 0 and 1 with setmaxnreg, 80 / 152):
+// hands registers to warpgroups 0-2 with setmaxnreg: 152, 152, 144 / 64):
 //   * warp 12    : TMA producer: K_j and V_j once; Q_i, dO_i (2-stage ring)
 //                  plus the 128 -LSE*log2e and -D values of tile i (bulk copies).
 //   * warp 13    : TMEM owner and single-thread tcgen05.mma issuer, per tile i:
@@ -31,9 +31,9 @@
 //                  dS^T = P^T o (dP^T - D) to shared memory (bf16/fp16,
 //                  128B-swizzled); at the end warpgroup 0 stores dK (x scale)
 //                  and warpgroup 1 stores dV.
-//   * warps 8-11 : one thread per query row: dQ_i from TMEM in 32-column
-//                  chunks, x scale, added into the fp32 accumulator with
-//                  vector reductions.
+//   * warps 8-11 : one thread per query row: dQ_i from TMEM (released as soon
+//                  as it is in registers), x scale, added into the fp32
+//                  accumulator with vector reductions.
 //   * warps 14-15: idle (they complete warpgroup 3 for the register split).
 //   * TMEM (512 columns): S^T/P^T [0,128) dP^T/dQ [128,256) dK [256,256+D)
 //                         dV [256+D,256+2D).
@@ -90,9 +90,9 @@ struct BwdCfg {
   static constexpr int THREADS = 512;
   static constexpr int REGS_LAUNCH = 128;
   static constexpr int REGS_MATH = 152;  // the two P / dS warpgroups
-  static constexpr int REGS_CTRL = 80;   // producer / MMA warpgroup
-  static_assert(128 * (2 * REGS_MATH + REGS_LAUNCH + REGS_CTRL) <= THREADS * REGS_LAUNCH,
-                "register split");
+  static constexpr int REGS_DQ = 144;    // the dQ warpgroup
+  static constexpr int REGS_CTRL = 64;   // producer / MMA warpgroup
+  static_assert(128 * (2 * REGS_MATH + REGS_DQ + REGS_CTRL) <= THREADS * REGS_LAUNCH, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DK = 256, T_DV = 256 + D;
   static_assert(256 + 2 * D <= 512, "TMEM budget");
@@ -286,51 +286,84 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     } else if (warp == 13 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
+      // Four chains over the query tiles i, each group issued as soon as ready:
+      //   S(i)  = K Q_i^T   needs Q_i resident and dV(i-1) complete (P^T aliases S^T)
+      //   dP(i) = V dO_i^T  needs dO_i resident and dQ(i-1) read out (dQ aliases dP^T)
+      //   dV(i)             needs P^T(i) in TMEM
+      //   dK(i), dQ(i)      need dS^T(i) in shared memory (and dV(i) issued)
       const uint32_t id_st = instr_desc_f16(128, 128, BF16, false, false, negate != 0);
       const uint32_t id_dpt = instr_desc_f16(128, 128, BF16, false, false);
       const uint32_t id_dv = instr_desc_f16(128, D, BF16, false, true);
       const uint32_t id_dk = instr_desc_f16(128, D, BF16, false, true);
       const uint32_t id_dq = instr_desc_f16(128, D, BF16, true, true);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, abort_flag, status);
-      for (int it = 0; ok && it < nq; ++it) {
-        const int s = it % C::NSTQ;
-        const uint32_t ph = (it / C::NSTQ) & 1;
-        const uint32_t q_s = sQ + s * C::TILE_BYTES, do_s = sDO + s * C::TILE_BYTES;
-        if (!(ok = mbar_wait(bar(C::B_QFULL + s), ph, abort_flag, status))) break;
-        if (it > 0 && !(ok = mbar_wait(bar(C::B_DVDONE), (it - 1) & 1, abort_flag, status))) break;
-        tc_fence_after_sync();
+      tc_fence_after_sync();
+      int is = 0, ip = 0, iv = 0, ik = 0;
+      uint64_t t_idle = global_timer_ns();
+      while (ok && ik < nq) {
+        bool progress = false;
+        if (ik < iv && ik < ip && mbar_probe(bar(C::B_DSFULL), ik & 1)) {
+          tc_fence_after_sync();
+          const uint32_t q_s = sQ + (ik % C::NSTQ) * C::TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::T_S, desc_k_tile<D>(sK, kk), desc_k_tile<D>(q_s, kk), id_st,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(bar(C::B_SFULL));
-        if (it > 0 && !(ok = mbar_wait(bar(C::B_DQEMPTY), (it - 1) & 1, abort_flag, status))) break;
-        tc_fence_after_sync();
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
+                   (ik > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + C::T_DP, desc_k_tile<D>(sV, kk), desc_k_tile<D>(do_s, kk), id_dpt,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(bar(C::B_DPFULL));
-        if (!(ok = mbar_wait(bar(C::B_PFULL), it & 1, abort_flag, status))) break;
-        tc_fence_after_sync();
+          for (int kk = 0; kk < C::BN / 16; ++kk)
+            mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(bar(C::B_DQFULL));
+          tc_commit(bar(C::B_QEMPTY + ik % C::NSTQ));
+          tc_commit(bar(C::B_DSEMPTY));
+          ++ik;
+          progress = true;
+        }
+        if (iv < is && mbar_probe(bar(C::B_PFULL), iv & 1)) {
+          tc_fence_after_sync();
+          const uint32_t do_s = sDO + (iv % C::NSTQ) * C::TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                 desc_mn_tile<D>(do_s, kk), id_dv, (it > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::B_DVDONE));
-        if (!(ok = mbar_wait(bar(C::B_DSFULL), it & 1, abort_flag, status))) break;
-        tc_fence_after_sync();
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                   desc_mn_tile<D>(do_s, kk), id_dv, (iv > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(C::B_DVDONE));
+          ++iv;
+          progress = true;
+        }
+        if (is < nq && is == iv && mbar_probe(bar(C::B_QFULL + is % C::NSTQ), (is / C::NSTQ) & 1) &&
+            (is == 0 || mbar_probe(bar(C::B_DVDONE), (is - 1) & 1))) {
+          tc_fence_after_sync();
+          const uint32_t q_s = sQ + (is % C::NSTQ) * C::TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::T_S, desc_k_tile<D>(sK, kk), desc_k_tile<D>(q_s, kk), id_st,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(bar(C::B_SFULL));
+          ++is;
+          progress = true;
+        }
+        if (ip < nq && ip == ik && mbar_probe(bar(C::B_QFULL + ip % C::NSTQ), (ip / C::NSTQ) & 1) &&
+            (ip == 0 || mbar_probe(bar(C::B_DQEMPTY), (ip - 1) & 1))) {
+          tc_fence_after_sync();
+          const uint32_t do_s = sDO + (ip % C::NSTQ) * C::TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(bar(C::B_DQFULL));
-        tc_commit(bar(C::B_QEMPTY + s));
-        tc_commit(bar(C::B_DSEMPTY));
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + C::T_DP, desc_k_tile<D>(sV, kk), desc_k_tile<D>(do_s, kk), id_dpt,
+                   kk > 0 ? 1u : 0u);
+          tc_commit(bar(C::B_DPFULL));
+          ++ip;
+          progress = true;
+        }
+        if (progress) {
+          t_idle = global_timer_ns();
+        } else if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
+          *abort_flag = 1;
+          ok = false;
+        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicExch(status, kStatusTimeout);
+          ok = false;
+        }
       }
       tc_commit(bar(C::B_MMADONE));
       drain_wait(bar(C::B_MMADONE), 0);
@@ -439,26 +472,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
   } else {
     // ----------------------------------------------- dQ, query rows (warps 8-11)
+    regs_increase<C::REGS_DQ>();
     const int t = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     for (int it = 0; it < nq; ++it) {
       const int qrow = (i0 + it) * C::BM + t;
       if (!mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status)) break;
       tc_fence_after_sync();
-      float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
+      uint32_t v[D];
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, v);
-        if (qrow < N) {
+        uint32_t w[32];
+        tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, w);
 #pragma unroll
-          for (int c = 0; c < 32; c += 4)
-            red_add_v4(dst + c0 * 32 + c, __uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
-                       __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
-        }
+        for (int i = 0; i < 32; ++i) v[c0 * 32 + i] = w[i];
       }
       tc_fence_before_sync();
-      mbar_arrive(bar(C::B_DQEMPTY));
+      mbar_arrive(bar(C::B_DQEMPTY));  // TMEM columns free for the next dP^T
+      if (qrow < N) {
+        float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 4)
+          red_add_v4(dst + c, __uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
+                     __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
+      }
     }
   }
 
