@@ -96,6 +96,33 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream);
 
 /*
+ * attn_bwd without any memory allocation (bf16).  The pages have no
+ * counterpart: this is a deployment variant of attn_bwd.
+ *
+ * For callers that may not allocate device memory inside the call: code that
+ * runs while an allocator must not be re-entered, runtimes that freeze device
+ * allocations once a fixed memory budget is set up, or hosts that give the
+ * library only the tensors.  Parameters, layouts, ownership and results are
+ * those of attn_bwd; the difference is where the scratch lives.  Instead of
+ * the stream-ordered allocator it uses one fixed 32 MiB array in device
+ * memory owned by the library (a GPU that loads the array keeps it until the
+ * process exits).  The scratch a problem needs is
+ *     align256(4*B*H*N*d) + 2 * align256(4*B*H*ceil(N/128)*128)   bytes;
+ * a problem needing more than 32 MiB is rejected with ATTN_ERR_UNSUPPORTED
+ * before anything is enqueued (use attn_bwd for it).
+ *   - The first call on each device looks up the array's device address on
+ *     that device; make that first call before any stream capture.
+ *   - Every call on a device shares the one array.  A call rewrites all of
+ *     the scratch it reads, so it does not depend on what an earlier call
+ *     left there, but two calls that can run at the same time on the GPU
+ *     (different streams, or different host threads) race on it and give
+ *     wrong gradients: order them on one stream or synchronise in between.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                     float scale, int causal, void* stream);
+
+/*
  * Synchronises `stream`, then returns and clears the sticky device status of
  * the current device (ATTN_OK, ATTN_ERR_TIMEOUT or ATTN_ERR_DEVICE_CHECK), or
  * ATTN_ERR_CUDA if the synchronisation itself failed.

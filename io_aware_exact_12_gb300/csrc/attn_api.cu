@@ -132,6 +132,12 @@ bool check_launch_regs(const void* func, int regs) {
   return fa.numRegs == regs;
 }
 
+int* status_word_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return status_ptr(dev);
+}
+
 BwdScratch bwd_scratch_layout(int BH, int N, int d) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t Npad = static_cast<size_t>((N + 127) / 128) * 128;

@@ -71,4 +71,8 @@ bool check_launch_regs(const void* func, int regs);
 int launch_fwd(const FwdArgs& a);
 int launch_bwd(const BwdArgs& a);
 
+// Device address of the sticky status word on the current device (nullptr on
+// failure).  Defined next to the word itself.
+int* status_word_current_device();
+
 }  // namespace attn
