@@ -87,10 +87,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def sources_sha():
+KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd.cu", "tc_sm103.cuh"),
+                  "attn_bwd_kernel": ("attn_bwd.cu", "tc_sm103.cuh")}
+
+
+def sources_sha(kernel):
+    """Short hash of the device source files a kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "io_aware_exact_12_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -105,7 +110,7 @@ def traffic_from_profiles(kernel, config_key):
         lines = open(path).read().splitlines()
     except OSError:
         return None
-    sha = sources_sha()
+    sha = sources_sha(kernel)
     for ln in lines:
         if ln.startswith("#") or not ln.strip():
             continue
