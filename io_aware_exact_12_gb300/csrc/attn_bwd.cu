@@ -25,15 +25,19 @@
 //                    dV  += P^T dO_i           (TS, P^T from TMEM, dO MN-major)
 //                    dK  += dS^T Q_i           (SS, dS^T K-major, Q MN-major)
 //                    dQ_i = dS K_j             (SS, dS MN-major view of the same
-//                                               shared tile, K MN-major)
+//                                               shared tile, K MN-major; at d = 128
+//                                               as dQ_i^T = K_j^T dS^T, operands swapped)
 //   * warps 0-7  : two threads per key row (warpgroup g takes query columns
 //                  64g..64g+63): P^T from S^T and LSE (exp2), P^T to TMEM,
 //                  dS^T = P^T o (dP^T - D) to shared memory (bf16/fp16,
 //                  128B-swizzled); at the end warpgroup 0 stores dK (x scale)
 //                  and warpgroup 1 stores dV.
-//   * warps 8-11 : one thread per query row: dQ_i from TMEM (released as soon
-//                  as it is in registers), x scale, added into the fp32
-//                  accumulator with vector reductions.
+//   * warps 8-11 : dQ_i from TMEM (released as soon as it is in registers),
+//                  x scale, added into the fp32 accumulator with reductions.
+//                  At d = 128 the MMA produces dQ_i^T = K_j^T dS^T instead, so a
+//                  thread holds one head-dim column and each warp-wide reduction
+//                  is 128 contiguous bytes of a dQ row (8x fewer L2 requests
+//                  than row-per-thread 16-byte vector reductions).
 //   * warps 14-15: idle (they complete warpgroup 3 for the register split).
 //   * TMEM (512 columns): S^T/P^T [0,128) dP^T/dQ [128,256) dK [256,256+D)
 //                         dV [256+D,256+2D).
@@ -95,6 +99,11 @@ struct BwdCfg {
   static_assert(128 * (2 * REGS_MATH + REGS_DQ + REGS_CTRL) <= THREADS * REGS_LAUNCH, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0, T_DP = 128, T_DK = 256, T_DV = 256 + D;
+  // d = 128: the MMA produces dQ^T = K^T dS^T (TMEM lane = head-dim index), so
+  // each warp's reduction into the accumulator covers 128 contiguous bytes of
+  // one dQ row.  Smaller d keeps dQ = dS K (lane = query row): an M = d < 128
+  // accumulator would use a different TMEM layout.
+  static constexpr bool DQ_T = (D == 128);
   static_assert(256 + 2 * D <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint32_t id_dpt = instr_desc_f16(128, 128, BF16, false, false);
       const uint32_t id_dv = instr_desc_f16(128, D, BF16, false, true);
       const uint32_t id_dk = instr_desc_f16(128, D, BF16, false, true);
-      const uint32_t id_dq = instr_desc_f16(128, D, BF16, true, true);
+      const uint32_t id_dq = instr_desc_f16(128, C::DQ_T ? 128 : D, BF16, true, true);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, abort_flag, status);
       tc_fence_after_sync();
       int is = 0, ip = 0, iv = 0, ik = 0;
@@ -310,9 +319,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
                    (ik > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk)
-            mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
-                   kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: both operands MN-major
+              mma_ss(tmem + C::T_DP, desc_mn_tile<D>(sK, kk), desc_ds_mnmajor(sDS, kk), id_dq,
+                     kk > 0 ? 1u : 0u);
+            else                    // dQ = dS K
+              mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
+                     kk > 0 ? 1u : 0u);
+          }
           tc_commit(bar(C::B_DQFULL));
           tc_commit(bar(C::B_QEMPTY + ik % C::NSTQ));
           tc_commit(bar(C::B_DSEMPTY));
@@ -471,17 +485,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     }
   } else {
-    // ----------------------------------------------- dQ, query rows (warps 8-11)
+    // ------------------------------------------------------ dQ (warps 8-11)
+    // DQ_T: thread t holds head-dim column t of dQ for the tile's 128 query
+    // rows; otherwise thread t holds query row t.
     regs_increase<C::REGS_DQ>();
     const int t = threadIdx.x & 127;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    constexpr int NCOL = C::DQ_T ? C::BM : D;
     for (int it = 0; it < nq; ++it) {
-      const int qrow = (i0 + it) * C::BM + t;
+      const int q0 = (i0 + it) * C::BM;
+      const int qrow = q0 + t;
       if (!mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status)) break;
       tc_fence_after_sync();
-      uint32_t v[D];
+      uint32_t v[NCOL];
 #pragma unroll
-      for (int c0 = 0; c0 < D / 32; ++c0) {
+      for (int c0 = 0; c0 < NCOL / 32; ++c0) {
         uint32_t w[32];
         tmem_ld32(tmem + lane_off + C::T_DP + c0 * 32, w);
 #pragma unroll
@@ -489,7 +507,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_DQEMPTY));  // TMEM columns free for the next dP^T
-      if (qrow < N) {
+      if constexpr (C::DQ_T) {
+        // one fp32 reduction per query row; the warp's 32 lanes are 32 adjacent
+        // head-dim columns, i.e. 128 contiguous bytes
+        float* dst = dq_acc + static_cast<int64_t>(bh) * N * D + static_cast<int64_t>(q0) * D + t;
+        const int nrow = min(C::BM, N - q0);
+#pragma unroll
+        for (int c = 0; c < C::BM; ++c)
+          if (c < nrow) red_add_f32(dst + static_cast<int64_t>(c) * D, __uint_as_float(v[c]) * scale);
+      } else if (qrow < N) {
         float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 4)
