@@ -373,7 +373,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
       // P is rounded to the input type for the P V product.
-      float2 se0 = make_float2(0.f, 0.f), se1 = se0, sr0 = se0, sr1 = se0;
+      float2 se0 = make_float2(0.f, 0.f), se1 = se0;
+      float sr0 = 0.f, sr1 = 0.f, sr2 = 0.f, sr3 = 0.f;
 #pragma unroll
       for (int c0 = 0; c0 < 2; ++c0) {
         uint32_t pk[32];
@@ -385,13 +386,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           pk[i + 1] = pack2<BF16>(p1.x, p1.y);
           se0 = add2(se0, p0);
           se1 = add2(se1, p1);
-          sr0 = add2(sr0, unpack2<BF16>(pk[i]));
-          sr1 = add2(sr1, unpack2<BF16>(pk[i + 1]));
+          if (i & 2) {
+            sr2 = add_halves<BF16>(sr2, pk[i]);
+            sr3 = add_halves<BF16>(sr3, pk[i + 1]);
+          } else {
+            sr0 = add_halves<BF16>(sr0, pk[i]);
+            sr1 = add_halves<BF16>(sr1, pk[i + 1]);
+          }
         }
         tmem_st32(tS + c0 * 32, pk);
       }
       l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
-      l_round = l_round * alpha + ((sr0.x + sr0.y) + (sr1.x + sr1.y));
+      l_round = l_round * alpha + ((sr0 + sr1) + (sr2 + sr3));
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL + q));

@@ -322,6 +322,22 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return d;
 }
 
+// acc + (both halves of a packed bf16x2 / f16x2 word), with the halves
+// converted exactly: mixed-precision f32 += 16-bit adds (sm_100 family).
+template <bool BF16>
+__device__ __forceinline__ float add_halves(float acc, uint32_t packed) {
+  if constexpr (BF16) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "+f"(acc) : "r"(packed));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %0, hi, %0;\n\t}"
+        : "+f"(acc) : "r"(packed));
+  }
+  return acc;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
