@@ -129,6 +129,17 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  */
 int attn_sync_status(void* stream);
 
+/*
+ * Self-test of the device failure path (the pages have no counterpart).
+ * Enqueues one tiny kernel that runs the library's bounded pipeline wait on a
+ * barrier nothing arrives on, with a limit of `limit_us` microseconds
+ * (1 .. 2,000,000).  The wait gives up, the kernel records ATTN_ERR_TIMEOUT
+ * in the sticky status and returns; a following attn_sync_status(stream)
+ * returns ATTN_ERR_TIMEOUT and clears it.  Nothing hangs or faults; the
+ * context stays usable.  Returns ATTN_OK if the kernel was enqueued.
+ */
+int attn_debug_wait_timeout(int limit_us, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_string(int status);
 

@@ -80,8 +80,9 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Returns false (and
 // raises the abort flag and device status) if it does not within the limit,
 // or if another role of the CTA, or another CTA, already failed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int* abort_flag, int* status,
+                                                uint64_t limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -91,12 +92,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       *abort_flag = 1;
       return false;
     }
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicExch(status, kStatusTimeout);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  return mbar_wait_limit(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
 // --------------------------------------------------------------------- TMA
