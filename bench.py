@@ -192,6 +192,40 @@ def oracle_sample(N, d, causal, seed, heads=1):
     return dt, f + b, threads
 
 
+DECODE = {"workload": "decode: 1 query token per (b, h) against a bf16 KV cache, B=16 H=16 L=32768 d=128",
+          "B": 16, "H": 16, "L": 32768, "d": 128}
+
+
+def measure_decode(attn, steps, warmup, peaks):
+    """Decode is bound by reading the cache: report GB/s of algorithmic bytes
+    (K and V once, q, o, lse) against the measured HBM copy bandwidth."""
+    import torch
+    B, H, L, d = DECODE["B"], DECODE["H"], DECODE["L"], DECODE["d"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    k = torch.randn((B, H, L, d), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((B, H, L, d), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    q = torch.randn((B, H, d), generator=g, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H), device="cuda", dtype=torch.float32)
+    for _ in range(max(warmup, 3)):
+        attn.attn_decode(q, k, v, o=o, lse=lse)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        attn.attn_decode(q, k, v, o=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = 2 * B * H * L * d * 2 + 2 * B * H * d * 2 + 4 * B * H
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    del k, v
+    return dict(DECODE, ms=ms, bytes_per_call=nbytes, gbs=gbs, bound="hbm", peak_gbs=peak, frac=gbs / peak,
+                status=attn.sync_status())
+
+
 def cpu_model():
     try:
         for ln in open("/proc/cpuinfo"):
@@ -353,6 +387,8 @@ def run_ours(args):
             "note": ("bwd duration is the whole attn_bwd call (preprocess + main + dQ convert), "
                      "so `achieved` understates the main kernel slightly") if dom_name == "bwd" else ""}
 
+    decode = measure_decode(attn, K, args.warmup, peaks) if rank == 0 else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, fl, threads = oracle_sample(N, d, causal, seed=4, heads=1)
@@ -370,7 +406,7 @@ def run_ours(args):
                 "causal": {"fwd_ms": statistics.median(cf_ms), "bwd_ms": statistics.median(cb_ms),
                            "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
                            "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
-                "roofline": roof, "cpu_baseline": cpu,
+                "roofline": roof, "cpu_baseline": cpu, "decode": decode,
                 "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "gpu_launches_e2e": launches_e2e,

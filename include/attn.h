@@ -96,6 +96,22 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream);
 
 /*
+ * Decode: exact attention of ONE query token per (batch, head) against a
+ * key/value cache of L tokens (bf16), all L keys visible.
+ *   q    : in,  [B, H, d] bf16 (the [B, H, 1, d] query of one decode step)
+ *   k, v : in,  [B, H, L, d] bf16 cache
+ *   o    : out, [B, H, d] bf16;  lse : out, [B, H] fp32
+ * The keys of each (b, h) are split across CTAs and the partial results
+ * (running max, sum, unnormalised output) merged exactly -- the decode
+ * variant named in FlashAttention (PKM page), "注意" section, with the
+ * online-softmax merge of "三招" 2.  Bound by reading the cache from HBM.
+ * Scratch: B*H*splits*(d+2) floats from cudaMallocAsync on `stream`, freed
+ * on it; launches 2 kernels.  Same conventions and errors as attn_fwd.
+ */
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int L, int d, float scale, void* stream);
+
+/*
  * attn_bwd without any memory allocation (bf16).  The pages have no
  * counterpart: this is a deployment variant of attn_bwd.
  *
@@ -143,8 +159,8 @@ int attn_debug_wait_timeout(int limit_us, void* stream);
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_string(int status);
 
-/* Number of kernel launches the most recent successful attn_fwd* / attn_bwd*
- * call on this thread enqueued (1 for the forward, 3 for the backward). */
+/* Number of kernel launches the most recent successful attn_fwd* / attn_bwd* /
+ * attn_decode call on this thread enqueued (forward 1, backward 3, decode 2). */
 int attn_last_launch_count(void);
 
 #ifdef __cplusplus

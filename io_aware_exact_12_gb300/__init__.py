@@ -19,7 +19,7 @@ import os
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
         for f in (L.attn_fwd, L.attn_fwd_f16, L.attn_bwd, L.attn_bwd_f16):
             f.restype = I
+        L.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
+        L.attn_decode.restype = I
         L.attn_sync_status.argtypes = [P]
         L.attn_sync_status.restype = I
         L.attn_status_string.argtypes = [I]
@@ -140,6 +142,35 @@ def attn_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
     if rc:
         raise AttnError("attn_bwd", rc)
     return dq, dk, dv
+
+
+def attn_decode(q, k, v, scale=None, o=None, lse=None, stream=None):
+    """One decode step: q [B, H, d] (or [B, H, 1, d]) against the cache k, v
+    [B, H, L, d], bf16; every key visible.  Returns (o [B, H, d], lse [B, H])."""
+    if q.dim() == 4:
+        if q.shape[2] != 1:
+            raise ValueError("decode takes one query token per (batch, head)")
+        q = q.reshape(q.shape[0], q.shape[1], q.shape[3])
+    if q.dim() != 3 or k.dim() != 4:
+        raise ValueError("q must be [B, H, d] and k, v [B, H, L, d]")
+    B, H, d = (int(x) for x in q.shape)
+    Lk = int(k.shape[2])
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(name, t, None, torch.bfloat16)
+    if tuple(k.shape) != (B, H, Lk, d) or tuple(v.shape) != (B, H, Lk, d):
+        raise ValueError("k and v must be [B, H, L, d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("o", o, q, torch.bfloat16)
+    _check("lse", lse, None, torch.float32)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Lk,
+                               d, float(scale), _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_decode", rc)
+    return o, lse
 
 
 def sync_status(stream=None) -> int:

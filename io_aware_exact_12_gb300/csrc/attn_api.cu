@@ -232,10 +232,50 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   return rc;
 }
 
+int decode_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int L, int d, float scale, void* stream) {
+  if (!q || !k || !v || !o || !lse) return kStatusInvalid;
+  int rc = validate_common(B, H, L, d, scale);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return kStatusInvalid;
+  const size_t qbytes = static_cast<size_t>(B) * H * d * 2;
+  const size_t kvbytes = qbytes * static_cast<size_t>(L);
+  const size_t lbytes = static_cast<size_t>(B) * H * 4;
+  for (const void* in : {q, k, v}) {
+    const size_t n = in == q ? qbytes : kvbytes;
+    if (overlaps(o, qbytes, in, n) || overlaps(lse, lbytes, in, n)) return kStatusInvalid;
+  }
+  if (overlaps(o, qbytes, lse, lbytes)) return kStatusInvalid;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  DecodeArgs a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.BH = B * H; a.L = L; a.d = d;
+  a.sl2 = scale * 1.4426950408889634f;
+  a.splits = decode_splits(a.BH, L);
+  a.stream = static_cast<cudaStream_t>(stream);
+  const size_t ws_bytes = static_cast<size_t>(a.BH) * a.splits * (d + 2) * sizeof(float);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, ws_bytes, a.stream) != cudaSuccess) return kStatusCuda;
+  a.ws = static_cast<float*>(ws);
+  rc = launch_decode(a);
+  const cudaError_t fe = cudaFreeAsync(ws, a.stream);
+  if (rc == kStatusOk && fe != cudaSuccess) rc = kStatusCuda;
+  if (rc == kStatusOk) t_last_launches = 2;
+  return rc;
+}
+
 }  // namespace
 }  // namespace attn
 
 extern "C" {
+
+int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int L, int d, float scale, void* stream) {
+  return attn::decode_entry(q, k, v, o, lse, B, H, L, d, scale, stream);
+}
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int N, int d, float scale, int causal, void* stream) {

@@ -68,7 +68,22 @@ bool ensure_smem_attr(const void* func, int bytes);
 // warpgroup register split that does not add up would wait forever).
 bool check_launch_regs(const void* func, int regs);
 
+struct DecodeArgs {
+  const void *q, *k, *v;  // q [BH][d], k/v [BH][L][d] bf16
+  void* o;                // [BH][d] bf16
+  float* lse;             // [BH]
+  int BH, L, d;
+  float sl2;              // scale * log2(e) (signed)
+  int splits;
+  cudaStream_t stream;
+  float* ws;              // [BH][splits][d + 2] fp32 partials
+};
+
+// Number of key splits per (batch, head) for a decode problem.
+int decode_splits(int BH, int L);
+
 int launch_fwd(const FwdArgs& a);
+int launch_decode(const DecodeArgs& a);
 int launch_bwd(const BwdArgs& a);
 
 // Device address of the sticky status word on the current device (nullptr on
