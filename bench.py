@@ -226,6 +226,40 @@ def measure_decode(attn, steps, warmup, peaks):
                 status=attn.sync_status())
 
 
+def measure_fp8(attn, steps, warmup, peaks):
+    """FP8 forward on the bench shape (B=2 H=16 N=8192 d=128), non-causal and
+    causal, against the fp8 dense peak = measured bf16 peak x 2 (the nominal
+    fp8/bf16 tensor-rate ratio, 4.5 / 2.25 PFLOP/s)."""
+    import torch
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs_fp8
+    B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
+    x = make_inputs_fp8(AttnShape(B, H, N, d), seed=4)
+    q8, k8, v8 = (x[n][0].cuda() for n in ("q", "k", "v"))
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    res = {"workload": "fp8 (e4m3) forward, B=2 H=16 N=8192 d=128, per-tensor descales", "peak_tflops": peak,
+           "peak_source": "measured bf16 x 2 (nominal fp8/bf16 ratio)"}
+    for causal in (False, True):
+        def run():
+            attn.attn_fwd_fp8(q8, k8, v8, x["q"][1], x["k"][1], x["v"][1], causal=causal, o=o, lse=lse)
+        for _ in range(max(warmup, 3)):
+            run()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        f, _ = flops_per_step(B, H, N, d, causal)
+        tf = f / (ms * 1e-3) / 1e12
+        res["causal" if causal else "noncausal"] = {"ms": ms, "tflops": tf, "frac": tf / peak}
+    res["status"] = attn.sync_status()
+    return res
+
+
 def cpu_model():
     try:
         for ln in open("/proc/cpuinfo"):
@@ -388,6 +422,7 @@ def run_ours(args):
                      "so `achieved` understates the main kernel slightly") if dom_name == "bwd" else ""}
 
     decode = measure_decode(attn, K, args.warmup, peaks) if rank == 0 else None
+    fp8 = measure_fp8(attn, K, args.warmup, peaks) if rank == 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -406,7 +441,7 @@ def run_ours(args):
                 "causal": {"fwd_ms": statistics.median(cf_ms), "bwd_ms": statistics.median(cb_ms),
                            "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
                            "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
-                "roofline": roof, "cpu_baseline": cpu, "decode": decode,
+                "roofline": roof, "cpu_baseline": cpu, "decode": decode, "fp8": fp8,
                 "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "gpu_launches_e2e": launches_e2e,

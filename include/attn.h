@@ -96,6 +96,21 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream);
 
 /*
+ * Forward with FP8 (e4m3) inputs: q, k, v are [B, H, N, 128] e4m3 bytes whose
+ * real values are descale_q*q, descale_k*k, descale_v*v (per-tensor factors,
+ * finite and > 0); o is bf16 [B, H, N, 128], lse fp32 [B, H, N] in the units
+ * of scale * Q_real K_real^T.  Same method as attn_fwd with 8-bit tensor-core
+ * MMAs (FlashAttention (PKM page) 效果 table / FA3 note: FP8 as the further
+ * gain); P is rounded to e4m3 for the P V product.  d must be 128 and
+ * scale >= 0 (else ATTN_ERR_UNSUPPORTED).  Scratch: a transposed copy of V,
+ * B*H*128*ceil(N/128)*128 bytes, from cudaMallocAsync on `stream` (freed on
+ * it); launches 2 kernels.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
+                 float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
+                 int causal, void* stream);
+
+/*
  * Decode: exact attention of ONE query token per (batch, head) against a
  * key/value cache of L tokens (bf16), all L keys visible.
  *   q    : in,  [B, H, d] bf16 (the [B, H, 1, d] query of one decode step)

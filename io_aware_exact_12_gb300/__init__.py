@@ -19,7 +19,7 @@ import os
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_fwd_fp8", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
         for f in (L.attn_fwd, L.attn_fwd_f16, L.attn_bwd, L.attn_bwd_f16):
             f.restype = I
+        L.attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, F, I, P]
+        L.attn_fwd_fp8.restype = I
         L.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
         L.attn_decode.restype = I
         L.attn_sync_status.argtypes = [P]
@@ -170,6 +172,32 @@ def attn_decode(q, k, v, scale=None, o=None, lse=None, stream=None):
                                d, float(scale), _stream_handle(stream))
     if rc:
         raise AttnError("attn_decode", rc)
+    return o, lse
+
+
+def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, scale=None, causal=False, o=None, lse=None,
+                 stream=None):
+    """Forward with e4m3 inputs (torch.float8_e4m3fn or uint8 views) and
+    per-tensor descale factors.  Returns (o bf16, lse fp32)."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, N, d]")
+    B, H, N, d = (int(x) for x in q.shape)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check(name, t, q)
+        if t.element_size() != 1:
+            raise TypeError("%s must hold one-byte e4m3 values" % name)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("o", o, None, torch.bfloat16)
+    _check("lse", lse, None, torch.float32)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), float(descale_q), float(descale_k),
+                                float(descale_v), o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
+                                int(bool(causal)), _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_fwd_fp8", rc)
     return o, lse
 
 

@@ -107,6 +107,19 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, i
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_map_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {stride1, stride2};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool ensure_smem_attr(const void* func, int bytes) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
@@ -267,10 +280,58 @@ int decode_entry(const void* q, const void* k, const void* v, void* o, float* ls
   return rc;
 }
 
+int fp8_entry(const void* q, const void* k, const void* v, float dq_s, float dk_s, float dv_s, void* o,
+              float* lse, int B, int H, int N, int d, float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return kStatusInvalid;
+  int rc = validate_common(B, H, N, d, scale);
+  if (rc) return rc;
+  if (!std::isfinite(dq_s) || !std::isfinite(dk_s) || !std::isfinite(dv_s) || dq_s <= 0.f ||
+      dk_s <= 0.f || dv_s <= 0.f)
+    return kStatusInvalid;
+  if (d != 128 || scale < 0.f) return kStatusUnsupported;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return kStatusInvalid;
+  const size_t ibytes = static_cast<size_t>(B) * H * N * d;  // one byte per input element
+  const size_t obytes = ibytes * 2, lbytes = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, obytes, in, ibytes) || overlaps(lse, lbytes, in, ibytes)) return kStatusInvalid;
+  if (overlaps(o, obytes, lse, lbytes)) return kStatusInvalid;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  int* st = status_ptr(dev);
+  if (!st) return kStatusCuda;
+  Fp8Args a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.BH = B * H; a.N = N; a.d = d;
+  a.sl2 = scale * dq_s * dk_s * 1.4426950408889634f;
+  a.descale_v = dv_s;
+  a.causal = causal ? 1 : 0;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = st;
+  const size_t Npad = static_cast<size_t>((N + 127) / 128) * 128;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, static_cast<size_t>(a.BH) * 128 * Npad, a.stream) != cudaSuccess)
+    return kStatusCuda;
+  a.ws_vt = static_cast<uint8_t*>(ws);
+  rc = launch_fwd_fp8(a);
+  const cudaError_t fe = cudaFreeAsync(ws, a.stream);
+  if (rc == kStatusOk && fe != cudaSuccess) rc = kStatusCuda;
+  if (rc == kStatusOk) t_last_launches = 2;
+  return rc;
+}
+
 }  // namespace
 }  // namespace attn
 
 extern "C" {
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
+                 float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
+                 int causal, void* stream) {
+  return attn::fp8_entry(q, k, v, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
+                         stream);
+}
 
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int L, int d, float scale, void* stream) {

@@ -79,6 +79,25 @@ struct DecodeArgs {
   float* ws;              // [BH][splits][d + 2] fp32 partials
 };
 
+struct Fp8Args {
+  const void *q, *k, *v;  // e4m3 [BH][N][128]
+  void* o;                // bf16 [BH][N][128]
+  float* lse;             // [BH][N]
+  int BH, N, d;
+  float sl2;              // scale * descale_q * descale_k * log2(e), >= 0
+  float descale_v;
+  int causal;
+  cudaStream_t stream;
+  int* status;
+  uint8_t* ws_vt;         // scratch V^T [BH][128][ceil(N/128)*128]
+};
+int launch_fwd_fp8(const Fp8Args& a);
+
+// 3-D tiled map over one-byte elements: dims (d0, d1, d2), byte strides of
+// dims 1 and 2, box (b0, b1, 1), 128-byte swizzle, zero fill.
+bool encode_map_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t stride1, uint64_t stride2, uint32_t b0, uint32_t b1);
+
 // Number of key splits per (batch, head) for a decode problem.
 int decode_splits(int BH, int L);
 

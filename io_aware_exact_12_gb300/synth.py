@@ -66,3 +66,37 @@ def sample_rows(shape: AttnShape, count: int, seed: int = 1234):
     bh = torch.cat([fixed_bh, bh])[:max(count, 4)]
     rows = torch.cat([fixed_rows, rows])[:max(count, 4)]
     return bh.numpy(), rows.numpy()
+
+
+E4M3_MAX = 448.0
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor e4m3 quantisation for FP8 inputs: descale = amax / 448 and
+    x8 = round-to-nearest-even(x / descale) in float8_e4m3fn, so that
+    descale * x8 approximates x.  Returns (x8 as uint8 bytes, descale).  The
+    real input both sides use is exactly descale * float(x8)."""
+    amax = float(x.abs().max())
+    descale = amax / E4M3_MAX if amax > 0 else 1.0
+    x8 = (x.float() / descale).to(torch.float8_e4m3fn)
+    return x8.view(torch.uint8).contiguous(), descale
+
+
+def make_inputs_fp8(shape: AttnShape, seed: int = 0, qk_std: float = 1.0):
+    """The make_inputs draws (fp32, same order and seed), each tensor then
+    quantised per tensor to e4m3.  Returns dict name -> (uint8 bytes, descale)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    dims = (shape.B, shape.H, shape.N, shape.d)
+    out = {}
+    for name in ("q", "k", "v"):
+        x = torch.randn(dims, generator=g, dtype=torch.float32)
+        if name in ("q", "k") and qk_std != 1.0:
+            x = x * qk_std
+        out[name] = quantize_e4m3(x)
+    return out
+
+
+def dequantize_e4m3(x8: torch.Tensor, descale: float) -> torch.Tensor:
+    """float64 real values descale * e4m3 (exact)."""
+    return x8.view(torch.float8_e4m3fn).double() * descale
