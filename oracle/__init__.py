@@ -44,13 +44,18 @@ def _load():
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         lib.oracle_forward.argtypes = [P, P, P, P, P, P, I64, I64, I64, ctypes.c_double, ctypes.c_int, ctypes.c_int]
+        lib.oracle_forward_masked.argtypes = [P, P, P, P, P, P, I64, I64, I64, ctypes.c_double, ctypes.c_int, P,
+                                              I64, I64, ctypes.c_int]
+        lib.oracle_backward_masked.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, ctypes.c_double,
+                                               ctypes.c_int, P, I64, I64, ctypes.c_int]
         lib.oracle_backward.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, ctypes.c_double, ctypes.c_int,
                                         ctypes.c_int]
         lib.oracle_rows.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_double, ctypes.c_int, P, P, I64, P, P, P,
                                     ctypes.c_int]
         lib.oracle_cols.argtypes = [P, P, P, P, P, P, I64, I64, I64, ctypes.c_double, ctypes.c_int, P, P, I64, P,
                                     P, ctypes.c_int]
-        for f in (lib.oracle_forward, lib.oracle_backward, lib.oracle_rows, lib.oracle_cols):
+        for f in (lib.oracle_forward, lib.oracle_backward, lib.oracle_rows, lib.oracle_cols,
+                  lib.oracle_forward_masked, lib.oracle_backward_masked):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -77,10 +82,22 @@ def _shape(q):
     return q.shape
 
 
-def forward(q, k, v, scale, causal, want_p=False, threads=None):
+def _mask(block_mask, H, N, blk):
+    if block_mask is None:
+        return None, 0
+    m = np.ascontiguousarray(np.asarray(block_mask), dtype=np.uint8)
+    nb = (N + blk - 1) // blk
+    if m.ndim != 3 or m.shape[1:] != (nb, nb) or m.shape[0] not in (1, H):
+        raise ValueError("block_mask must be [H or 1, ceil(N/blk), ceil(N/blk)]")
+    return m, m.shape[0]
+
+
+def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None, blk=128):
     """O, LSE (and optionally P) of softmax(scale q k^T [+ causal mask]) v.
 
     q, k, v: [B, H, N, d] (any float dtype; upcast exactly to float64).
+    block_mask: optional [H or 1, nb, nb] (nb = ceil(N/blk)); key j is hidden
+    from query i unless block_mask[h][i // blk][j // blk] is nonzero.
     Returns (o [B,H,N,d], lse [B,H,N]) or (o, lse, p [B,H,N,N]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -88,20 +105,32 @@ def forward(q, k, v, scale, causal, want_p=False, threads=None):
     o = np.empty_like(q)
     lse = np.empty((B, H, N), dtype=np.float64)
     p = np.empty((B, H, N, N), dtype=np.float64) if want_p else None
-    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H, N, d,
-                                float(scale), int(bool(causal)), threads or default_threads())
+    m, mh = _mask(block_mask, H, N, blk)
+    if m is None:
+        rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H, N, d,
+                                    float(scale), int(bool(causal)), threads or default_threads())
+    else:
+        rc = _load().oracle_forward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H, N, d,
+                                           float(scale), int(bool(causal)), _ptr(m), mh, blk,
+                                           threads or default_threads())
     if rc:
         raise RuntimeError("oracle_forward failed (%d)" % rc)
     return (o, lse, p) if want_p else (o, lse)
 
 
-def backward(q, k, v, o, do, scale, causal, threads=None):
+def backward(q, k, v, o, do, scale, causal, threads=None, block_mask=None, blk=128):
     """dQ, dK, dV of L = <O, dO>; ``o`` is the oracle's own forward output."""
     q, k, v, o, do = (_f64(x) for x in (q, k, v, o, do))
     B, H, N, d = _shape(q)
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
-    rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
-                                 B * H, N, d, float(scale), int(bool(causal)), threads or default_threads())
+    m, mh = _mask(block_mask, H, N, blk)
+    if m is None:
+        rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                                     B * H, N, d, float(scale), int(bool(causal)), threads or default_threads())
+    else:
+        rc = _load().oracle_backward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq), _ptr(dk),
+                                            _ptr(dv), B * H, N, d, float(scale), int(bool(causal)), _ptr(m), mh,
+                                            blk, threads or default_threads())
     if rc:
         raise RuntimeError("oracle_backward failed (%d)" % rc)
     return dq, dk, dv

@@ -33,6 +33,12 @@
  * Layout: every [B,H,N,d] tensor is row-major float64, viewed as BH = B*H
  * independent heads of [N][d]; lse is [BH][N].
  *
+ * Block-sparse variant (FlashAttention深度攻略, 进阶追问 "Sparse FlashAttention"
+ * and its note separating tiling from block-sparse attention): an optional
+ * mask [mask_heads][nb][nb] of bytes, head h using mask h % mask_heads, hides
+ * key j from query i unless mask[i / blk][j / blk] != 0 (on top of the causal
+ * rule).  A row that sees no key at all has O = 0 and LSE = -inf.
+ *
  * Work is spread over threads by (head, block of rows) or (head, block of key
  * columns); each row or column is computed exactly as the definition reads,
  * so threading changes no arithmetic.
@@ -52,6 +58,9 @@ typedef struct {
   int64_t BH, N, d;
   double scale;
   int causal;
+  /* optional block mask */
+  const uint8_t *bmask;
+  int64_t mask_heads, nb, blk;
   /* sampled rows / columns */
   const int64_t *bh_idx, *idx;
   int64_t nsel;
@@ -83,18 +92,35 @@ static int run_threads(void *(*fn)(void *), job_t *j, int nthreads) {
   return 0;
 }
 
+/* Visibility rule of one query row: causal flag and (optional) its row of the block mask. */
+typedef struct {
+  int causal;
+  const uint8_t *mrow; /* mask row of query i's block (nb entries) or NULL */
+  int64_t blk;
+} vis_t;
+
 /* Is key j visible to query i? */
-static int visible(int causal, int64_t i, int64_t j) { return !causal || j <= i; }
+static int visible(vis_t v, int64_t i, int64_t j) {
+  return (!v.causal || j <= i) && (!v.mrow || v.mrow[j / v.blk]);
+}
+
+static vis_t vis_for(const job_t *J, int64_t h, int64_t i) {
+  vis_t v;
+  v.causal = J->causal;
+  v.blk = J->blk;
+  v.mrow = J->bmask ? J->bmask + ((h % J->mask_heads) * J->nb + i / J->blk) * J->nb : NULL;
+  return v;
+}
 
 /* One query row of one head, materialising its row of S and P.
  * s_row, p_row: scratch of length N.  Writes o_row[d], *lse_out, and p_row. */
 static void forward_row(const double *qh, const double *kh, const double *vh, int64_t N,
-                        int64_t d, double scale, int causal, int64_t i, double *s_row,
+                        int64_t d, double scale, vis_t vis, int64_t i, double *s_row,
                         double *p_row, double *o_row, double *lse_out) {
   const double *qi = qh + i * d;
   double m = -INFINITY;
   for (int64_t j = 0; j < N; ++j) {
-    if (!visible(causal, i, j)) {
+    if (!visible(vis, i, j)) {
       s_row[j] = -INFINITY;
       continue;
     }
@@ -103,6 +129,12 @@ static void forward_row(const double *qh, const double *kh, const double *vh, in
     for (int64_t c = 0; c < d; ++c) acc += qi[c] * kj[c];
     s_row[j] = scale * acc;
     if (s_row[j] > m) m = s_row[j];
+  }
+  if (m == -INFINITY) { /* no visible key: O = 0, LSE = -inf */
+    for (int64_t j = 0; j < N; ++j) p_row[j] = 0.0;
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    *lse_out = -INFINITY;
+    return;
   }
   double l = 0.0;
   for (int64_t j = 0; j < N; ++j) {
@@ -132,7 +164,7 @@ static void *fwd_worker(void *arg) {
     const double *qh = J->q + h * N * d, *kh = J->k + h * N * d, *vh = J->v + h * N * d;
     for (int64_t i = rb * ROWS_PER_ITEM; i < N && i < (rb + 1) * ROWS_PER_ITEM; ++i) {
       double *p_row = J->p_out ? J->p_out + (h * N + i) * N : p_tmp;
-      forward_row(qh, kh, vh, N, d, J->scale, J->causal, i, s_row, p_row,
+      forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), i, s_row, p_row,
                   J->o_out + (h * N + i) * d, J->lse_out + h * N + i);
     }
   }
@@ -143,12 +175,16 @@ static void *fwd_worker(void *arg) {
 
 /* O = softmax(scale Q K^T [+ causal mask]) V and LSE for all heads.
  * p_out: optional [BH][N][N] probabilities (NULL to skip). */
-int oracle_forward(const double *q, const double *k, const double *v, double *o, double *lse,
-                   double *p_out, int64_t BH, int64_t N, int64_t d, double scale, int causal,
-                   int nthreads) {
+int oracle_forward_masked(const double *q, const double *k, const double *v, double *o,
+                          double *lse, double *p_out, int64_t BH, int64_t N, int64_t d,
+                          double scale, int causal, const uint8_t *bmask, int64_t mask_heads,
+                          int64_t blk, int nthreads) {
   if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !lse) return 1;
+  if (bmask && (mask_heads < 1 || blk < 1)) return 1;
   job_t J;
   memset(&J, 0, sizeof J);
+  J.bmask = bmask; J.mask_heads = mask_heads; J.blk = blk > 0 ? blk : 1;
+  J.nb = (N + J.blk - 1) / J.blk;
   J.q = q; J.k = k; J.v = v; J.o_out = o; J.lse_out = lse; J.p_out = p_out;
   J.BH = BH; J.N = N; J.d = d; J.scale = scale; J.causal = causal;
   J.nitems = BH * ((N + ROWS_PER_ITEM - 1) / ROWS_PER_ITEM);
@@ -156,6 +192,13 @@ int oracle_forward(const double *q, const double *k, const double *v, double *o,
   run_threads(fwd_worker, &J, nthreads);
   pthread_mutex_destroy(&J.mu);
   return 0;
+}
+
+int oracle_forward(const double *q, const double *k, const double *v, double *o, double *lse,
+                   double *p_out, int64_t BH, int64_t N, int64_t d, double scale, int causal,
+                   int nthreads) {
+  return oracle_forward_masked(q, k, v, o, lse, p_out, BH, N, d, scale, causal, NULL, 0, 0,
+                               nthreads);
 }
 
 /* --------------------------------------------------------------- backward */
@@ -172,7 +215,7 @@ static void *bwd_rows_worker(void *arg) {
     for (int64_t i = it * ROWS_PER_ITEM; i < N && i < (it + 1) * ROWS_PER_ITEM; ++i) {
       double *p_row = J->P_head + i * N, *ds_row = J->dS_head + i * N;
       double lse_unused;
-      forward_row(qh, kh, vh, N, d, J->scale, J->causal, i, s_row, p_row, o_row, &lse_unused);
+      forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), i, s_row, p_row, o_row, &lse_unused);
       const double *doi = doh + i * d, *oi = oh + i * d;
       double Di = 0.0;
       for (int64_t c = 0; c < d; ++c) Di += doi[c] * oi[c];
@@ -224,12 +267,16 @@ static void *bwd_cols_worker(void *arg) {
 /* Analytic backward.  o must be the forward output of the same inputs (the
  * oracle's own float64 O).  Materialises P and dS one head at a time
  * (2 * N * N doubles). */
-int oracle_backward(const double *q, const double *k, const double *v, const double *o,
-                    const double *dO, double *dq, double *dk, double *dv, int64_t BH, int64_t N,
-                    int64_t d, double scale, int causal, int nthreads) {
+int oracle_backward_masked(const double *q, const double *k, const double *v, const double *o,
+                           const double *dO, double *dq, double *dk, double *dv, int64_t BH,
+                           int64_t N, int64_t d, double scale, int causal, const uint8_t *bmask,
+                           int64_t mask_heads, int64_t blk, int nthreads) {
   if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !dO || !dq || !dk || !dv) return 1;
+  if (bmask && (mask_heads < 1 || blk < 1)) return 1;
   job_t J;
   memset(&J, 0, sizeof J);
+  J.bmask = bmask; J.mask_heads = mask_heads; J.blk = blk > 0 ? blk : 1;
+  J.nb = (N + J.blk - 1) / J.blk;
   J.q = q; J.k = k; J.v = v; J.o = o; J.dO = dO; J.dq = dq; J.dk = dk; J.dv = dv;
   J.BH = BH; J.N = N; J.d = d; J.scale = scale; J.causal = causal;
   J.P_head = (double *)malloc(sizeof(double) * N * N);
@@ -250,6 +297,13 @@ int oracle_backward(const double *q, const double *k, const double *v, const dou
   return 0;
 }
 
+int oracle_backward(const double *q, const double *k, const double *v, const double *o,
+                    const double *dO, double *dq, double *dk, double *dv, int64_t BH, int64_t N,
+                    int64_t d, double scale, int causal, int nthreads) {
+  return oracle_backward_masked(q, k, v, o, dO, dq, dk, dv, BH, N, d, scale, causal, NULL, 0, 0,
+                                nthreads);
+}
+
 /* ------------------------------------------------------- sampled query rows */
 
 /* For each selected (head, row) pair: O row, LSE and dQ row, straight from the
@@ -265,7 +319,7 @@ static void *rows_worker(void *arg) {
     const int64_t h = J->bh_idx[r], i = J->idx[r];
     const double *qh = J->q + h * N * d, *kh = J->k + h * N * d, *vh = J->v + h * N * d;
     double *oi = J->o_out + r * d;
-    forward_row(qh, kh, vh, N, d, J->scale, J->causal, i, s_row, p_row, oi, J->lse_out + r);
+    forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), i, s_row, p_row, oi, J->lse_out + r);
     if (!J->dq) continue;
     const double *doi = J->dO + (h * N + i) * d;
     double Di = 0.0;
@@ -323,7 +377,7 @@ static void *cols_worker(void *arg) {
     double *dkj = J->dk + r * d, *dvj = J->dv + r * d;
     for (int64_t c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
     for (int64_t i = 0; i < N; ++i) {
-      if (!visible(J->causal, i, j)) continue;
+      if (!visible(vis_for(J, h, i), i, j)) continue;
       const double *qi = qh + i * d, *doi = doh + i * d;
       double acc = 0.0, dp = 0.0;
       for (int64_t c = 0; c < d; ++c) { acc += qi[c] * kj[c]; dp += doi[c] * vj[c]; }

@@ -27,9 +27,11 @@ from __future__ import annotations
 import numpy as np
 
 
-def attention_blockwise(q, k, v, scale, causal, br=32, bc=32, trace=None):
+def attention_blockwise(q, k, v, scale, causal, br=32, bc=32, trace=None, mask_fn=None):
     """q: [N, d], k, v: [Nk, d] float64 for one head.  Returns (o [N, d], lse [N]).
 
+    ``mask_fn(i, j)``: optional visibility rule on index arrays (True = key j
+    visible to query i), applied on top of the causal rule.
     ``trace``: optional list; for each (query block, key block) step the
     rescale factors exp(m_{j-1} - m_j) of that step are appended, so a test
     can observe the correction the pages describe.
@@ -56,6 +58,8 @@ def attention_blockwise(q, k, v, scale, causal, br=32, bc=32, trace=None):
             if causal:
                 cols = np.arange(c0, c1)[None, :]
                 s = np.where(cols > rows, -np.inf, s)
+            if mask_fn is not None:  # mask_fn(i, j) -> bool arrays: is key j visible to query i
+                s = np.where(mask_fn(rows, np.arange(c0, c1)[None, :]), s, -np.inf)
             m_new = np.maximum(m, s.max(axis=1))
             # rows whose keys so far are all hidden keep m = -inf; guard exp(-inf - -inf)
             safe = np.where(np.isfinite(m_new), m_new, 0.0)
@@ -66,8 +70,9 @@ def attention_blockwise(q, k, v, scale, causal, br=32, bc=32, trace=None):
             if trace is not None:
                 trace.append(corr.copy())
             m = m_new
-        o_out[r0:r1] = acc / l[:, None]
-        lse_out[r0:r1] = m + np.log(l)
+        seen = l > 0  # rows that saw no key at all: O = 0, LSE = -inf
+        o_out[r0:r1] = np.where(seen[:, None], acc / np.where(seen, l, 1.0)[:, None], 0.0)
+        lse_out[r0:r1] = np.where(seen, m + np.log(np.where(seen, l, 1.0)), -np.inf)
     return o_out, lse_out
 
 

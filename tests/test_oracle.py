@@ -263,3 +263,91 @@ def test_oracle_rejects_bad_arguments():
         oracle.rows(x["q"], x["k"], x["v"], None, 1.0, False, np.array([1]), np.array([0]))
     with pytest.raises(RuntimeError):
         oracle.rows(x["q"], x["k"], x["v"], None, 1.0, False, np.array([0]), np.array([4]))
+
+
+# ------------------------------------------------------- block-sparse mask
+def _block_lower(nb):
+    return np.tril(np.ones((nb, nb), dtype=np.uint8))[None]
+
+
+def test_mask_all_ones_is_the_unmasked_definition():
+    x = _np_inputs(1, 2, 200, 16, seed=31)
+    for causal in (False, True):
+        o, l = oracle.forward(x["q"], x["k"], x["v"], 0.3, causal)
+        om, lm = oracle.forward(x["q"], x["k"], x["v"], 0.3, causal, block_mask=np.ones((1, 4, 4), np.uint8),
+                                blk=64)
+        np.testing.assert_array_equal(om, o)
+        np.testing.assert_array_equal(lm, l)
+
+
+def test_lower_block_mask_with_causal_is_causal():
+    x = _np_inputs(1, 2, 150, 8, seed=32)
+    o, l = oracle.forward(x["q"], x["k"], x["v"], 0.3, True)
+    om, lm = oracle.forward(x["q"], x["k"], x["v"], 0.3, True, block_mask=_block_lower(5), blk=32)
+    np.testing.assert_array_equal(om, o)
+    np.testing.assert_array_equal(lm, l)
+
+
+def test_block_diagonal_mask_is_independent_blocks():
+    """Only diagonal blocks visible = each block of rows attends only to its own
+    block of keys, i.e. independent attention problems of length blk."""
+    blk, nb = 16, 5
+    N = blk * nb - 7  # ragged last block
+    x = _np_inputs(1, 3, N, 8, seed=33)
+    mask = np.eye(nb, dtype=np.uint8)[None].repeat(3, 0)
+    om, lm = oracle.forward(x["q"], x["k"], x["v"], 0.4, False, block_mask=mask, blk=blk)
+    for b0 in range(0, N, blk):
+        sl = slice(b0, min(b0 + blk, N))
+        ob, lb = oracle.forward(x["q"][:, :, sl], x["k"][:, :, sl], x["v"][:, :, sl], 0.4, False)
+        np.testing.assert_allclose(om[:, :, sl], ob, rtol=1e-14, atol=1e-15)
+        np.testing.assert_allclose(lm[:, :, sl], lb, rtol=1e-15)
+
+
+def test_row_with_no_visible_block_is_zero_with_minus_inf_lse():
+    x = _np_inputs(1, 1, 64, 8, seed=34)
+    mask = np.ones((1, 4, 4), np.uint8)
+    mask[0, 2, :] = 0
+    om, lm = oracle.forward(x["q"], x["k"], x["v"], 0.4, False, block_mask=mask, blk=16)
+    assert (om[0, 0, 32:48] == 0).all() and np.isneginf(lm[0, 0, 32:48]).all()
+    assert np.isfinite(lm[0, 0, :32]).all() and np.isfinite(lm[0, 0, 48:]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_masked_oracle_matches_blockwise_reference(causal):
+    blk, N = 32, 150
+    nb = (N + blk - 1) // blk
+    rng = np.random.default_rng(35)
+    mask = (rng.random((2, nb, nb)) < 0.5).astype(np.uint8)
+    mask[:, np.arange(nb), np.arange(nb)] = 1
+    x = _np_inputs(1, 2, N, 16, seed=36)
+    om, lm = oracle.forward(x["q"], x["k"], x["v"], 0.25, causal, block_mask=mask, blk=blk)
+    for h in range(2):
+        fn = lambda i, j, h=h: mask[h][i // blk, j // blk].astype(bool)  # noqa: E731
+        ob, lb = attention_blockwise(x["q"][0, h], x["k"][0, h], x["v"][0, h], 0.25, causal, 16, 24,
+                                     mask_fn=fn)
+        np.testing.assert_allclose(om[0, h], ob, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lm[0, h], lb, rtol=1e-12, atol=1e-12)
+
+
+def test_masked_backward_matches_finite_differences():
+    rng = np.random.default_rng(37)
+    q, k, v, do = (rng.standard_normal((1, 1, 6, 2)) for _ in range(4))
+    mask = np.array([[[1, 0, 1], [0, 1, 1], [1, 1, 0]]], dtype=np.uint8)  # blk = 2
+    o, _ = oracle.forward(q, k, v, 0.7, False, block_mask=mask, blk=2)
+    dq, dk, dv = oracle.backward(q, k, v, o, do, 0.7, False, block_mask=mask, blk=2)
+
+    def loss(qq, kk, vv):
+        oo, _ = oracle.forward(qq, kk, vv, 0.7, False, threads=1, block_mask=mask, blk=2)
+        return float((oo * do).sum())
+
+    h = 1e-6
+    for name, grad in (("q", dq), ("k", dk), ("v", dv)):
+        base = {"q": q, "k": k, "v": v}
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            plus = {n: a.copy() for n, a in base.items()}
+            minus = {n: a.copy() for n, a in base.items()}
+            plus[name][idx] += h
+            minus[name][idx] -= h
+            fd[idx] = (loss(plus["q"], plus["k"], plus["v"]) - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=name)
