@@ -96,6 +96,21 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream);
 
 /*
+ * Block-sparse forward (bf16): attn_fwd where whole 128 x 128 tiles of the
+ * score matrix are enabled or skipped by a block mask (FlashAttention深度攻略,
+ * 进阶追问 "Sparse FlashAttention"; the tiles skipped are never loaded or
+ * multiplied, generalising the causal tile skipping).
+ *   block_mask : DEVICE pointer, [mask_heads][nb][nb] bytes, nb = ceil(N/128);
+ *                head h uses mask (h % H) % mask_heads, mask_heads in {1, H}.
+ *                Key j is visible to query i iff
+ *                block_mask[..][i / 128][j / 128] != 0 (and j <= i if causal).
+ *   A row that sees no key gets O = 0 and LSE = -inf.  N <= 65536.
+ */
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                         float scale, int causal, void* stream);
+
+/*
  * Forward with FP8 (e4m3) inputs: q, k, v are [B, H, N, 128] e4m3 bytes whose
  * real values are descale_q*q, descale_k*k, descale_v*v (per-tensor factors,
  * finite and > 0); o is bf16 [B, H, N, 128], lse fp32 [B, H, N] in the units

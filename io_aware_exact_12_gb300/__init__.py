@@ -19,7 +19,7 @@ import os
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_fwd_fp8", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
         for f in (L.attn_fwd, L.attn_fwd_f16, L.attn_bwd, L.attn_bwd_f16):
             f.restype = I
+        L.attn_fwd_blocksparse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, P]
+        L.attn_fwd_blocksparse.restype = I
         L.attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, F, I, P]
         L.attn_fwd_fp8.restype = I
         L.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
@@ -172,6 +174,35 @@ def attn_decode(q, k, v, scale=None, o=None, lse=None, stream=None):
                                d, float(scale), _stream_handle(stream))
     if rc:
         raise AttnError("attn_decode", rc)
+    return o, lse
+
+
+def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, lse=None, stream=None):
+    """Forward restricted by a block mask: block_mask is a uint8 CUDA tensor
+    [H or 1, ceil(N/128), ceil(N/128)]; key j is visible to query i iff
+    block_mask[h][i // 128][j // 128] != 0 (and j <= i if causal).
+    Returns (o, lse); rows that see no key get O = 0, LSE = -inf."""
+    B, H, N, d = _dims(q)
+    _check("q", q, None, torch.bfloat16)
+    _check("k", k, q, torch.bfloat16)
+    _check("v", v, q, torch.bfloat16)
+    nb = (N + 127) // 128
+    if (not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda or block_mask.dtype != torch.uint8
+            or not block_mask.is_contiguous() or block_mask.dim() != 3
+            or tuple(block_mask.shape[1:]) != (nb, nb) or block_mask.shape[0] not in (1, H)):
+        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [H or 1, %d, %d]" % (nb, nb))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check("o", o, q, torch.bfloat16)
+    _check("lse", lse, None, torch.float32)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                        block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
+                                        int(bool(causal)), _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_fwd_blocksparse", rc)
     return o, lse
 
 

@@ -245,6 +245,44 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   return rc;
 }
 
+int blocksparse_entry(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const uint8_t* mask, int mask_heads, int B, int H, int N, int d, float scale,
+                      int causal, void* stream) {
+  if (!mask) return kStatusInvalid;
+  if (mask_heads != 1 && mask_heads != H) return kStatusInvalid;
+  if ((N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+  if (!q || !k || !v || !o || !lse) return kStatusInvalid;
+  int rc = validate_common(B, H, N, d, scale);
+  if (rc) return rc;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return kStatusInvalid;
+  const size_t nbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, nbytes, in, nbytes) || overlaps(lse, lbytes, in, nbytes)) return kStatusInvalid;
+  if (overlaps(o, nbytes, lse, lbytes)) return kStatusInvalid;
+  int dev = 0;
+  if ((rc = current_device(&dev))) return rc;
+  int* st = status_ptr(dev);
+  if (!st) return kStatusCuda;
+  FwdArgs a;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse;
+  a.BH = B * H; a.N = N; a.d = d;
+  a.sl2 = std::fabs(scale) * 1.4426950408889634f;
+  a.causal = causal ? 1 : 0;
+  a.negate = scale < 0.f ? 1 : 0;
+  a.bf16 = true;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = st;
+  a.bmask = mask;
+  a.H = H;
+  a.mask_heads = mask_heads;
+  rc = launch_fwd(a);
+  if (rc == kStatusOk) t_last_launches = 1;
+  return rc;
+}
+
 int decode_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int L, int d, float scale, void* stream) {
   if (!q || !k || !v || !o || !lse) return kStatusInvalid;
@@ -331,6 +369,13 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
                  int causal, void* stream) {
   return attn::fp8_entry(q, k, v, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
                          stream);
+}
+
+int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                         float scale, int causal, void* stream) {
+  return attn::blocksparse_entry(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, scale, causal,
+                                 stream);
 }
 
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

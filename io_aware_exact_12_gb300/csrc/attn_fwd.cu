@@ -71,7 +71,10 @@ struct FwdCfg {
   static constexpr int NBAR = B_MMADONE + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
-  static constexpr int SMEM_BYTES = OFF_ABORT + 12;
+  static constexpr int OFF_NPOS = OFF_ABORT + 4;                   // int[3]: positions, per-tile counts
+  static constexpr int OFF_LIST = OFF_NPOS + 16;                   // uint16 key tile of each position
+  static constexpr int OFF_FLAGS = OFF_LIST + 2 * kMaxSparseTiles;  // uint8 bit q: tile q uses it
+  static constexpr int SMEM_BYTES = OFF_FLAGS + kMaxSparseTiles;
   static constexpr int THREADS = 384;
   static constexpr int REGS_LAUNCH = 168;   // 65536 / 384, rounded down to a multiple of 8
   static constexpr int REGS_MATH = 224;     // softmax warpgroups
@@ -107,13 +110,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D, bool BF16>
+// The key/value tiles a CTA visits are "positions" 0..npos-1: dense, position
+// p is key tile p and query tile q uses positions p < nkv[q]; block-sparse
+// (SPARSE), the positions are the union of the key tiles either query tile's
+// mask row enables (after the causal limit), listed in shared memory with a
+// per-position bit for each query tile.  Producer, MMA issuer and softmax all
+// walk positions, so a K/V tile is loaded once per CTA and each query tile
+// runs its S/PV chain over its own positions only.
+template <int D, bool BF16, bool SPARSE>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, uint8_t* __restrict__ o_out,
                     float* __restrict__ lse_out, int N, float sl2, int causal, int negate,
-                    int* status) {
+                    const uint8_t* __restrict__ bmask, int H, int mask_heads, int* status) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -139,7 +149,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMSLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
 
+  uint16_t* pos_tile = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST);
+  uint8_t* pos_flags = smem + C::OFF_FLAGS;
+  int* npos_slot = reinterpret_cast<int*>(smem + C::OFF_NPOS);
   if (threadIdx.x == 0) {
+    if constexpr (SPARSE) {
+      const uint8_t* mb = bmask + static_cast<size_t>((bh % H) % mask_heads) * nkv_all * nkv_all;
+      int n = 0, c0 = 0, c1 = 0;
+      for (int j = 0; j < nkv_all; ++j) {
+        int f = 0;
+        if (j < nkv[0] && mb[static_cast<size_t>(2 * qb) * nkv_all + j]) f |= 1;
+        if (j < nkv[1] && mb[static_cast<size_t>(2 * qb + 1) * nkv_all + j]) f |= 2;
+        if (f) {
+          pos_tile[n] = static_cast<uint16_t>(j);
+          pos_flags[n] = static_cast<uint8_t>(f);
+          c0 += f & 1;
+          c1 += f >> 1;
+          ++n;
+        }
+      }
+      npos_slot[0] = n;
+      npos_slot[1] = c0;
+      npos_slot[2] = c1;
+    }
     mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
@@ -168,6 +200,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const uint32_t sQ = sbase + C::OFF_Q;
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
+  const int npos = SPARSE ? npos_slot[0] : nkv_max;
+  int cnt[2];
+  cnt[0] = SPARSE ? npos_slot[1] : nkv[0];
+  cnt[1] = SPARSE ? npos_slot[2] : nkv[1];
+  auto kv_tile = [&](int p) -> int { return SPARSE ? static_cast<int>(pos_tile[p]) : p; };
+  auto uses = [&](int q, int p) -> bool { return SPARSE ? ((pos_flags[p] >> q) & 1) != 0 : p < nkv[q]; };
 
   if (warp >= 8) {
     regs_decrease<C::REGS_CTRL>();
@@ -176,19 +214,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
-      for (int q = 0; q < 2; ++q)
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sQ + q * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), c * C::CH,
-                      qb * 2 * C::BM + q * C::BM, bh);
+      if (npos > 0) {  // a CTA with nothing to visit loads nothing
+        mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
+        for (int q = 0; q < 2; ++q)
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sQ + q * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), c * C::CH,
+                        qb * 2 * C::BM + q * C::BM, bh);
+      }
       int issued = 0;
-      for (int j = 0; j < nkv_max; ++j) {
+      for (int j = 0; j < npos; ++j) {
         const int s = j % C::NST, u = j / C::NST;
+        const int kv_row0 = kv_tile(j) * C::BN;
         if (u > 0 && !mbar_wait(bar(C::B_KEMPTY + s), (u - 1) & 1, abort_flag, status)) break;
         mbar_arrive_expect_tx(bar(C::B_KFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + s),
-                      c * C::CH, j * C::BN, bh);
+                      c * C::CH, kv_row0, bh);
         if (u > 0 && !mbar_wait(bar(C::B_VEMPTY + s), (u - 1) & 1, abort_flag, status)) {
           issued = -(j + 1);  // K_j issued, V_j not
           break;
@@ -196,12 +237,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(bar(C::B_VFULL + s), C::TILE_BYTES);
         for (int c = 0; c < C::NCH; ++c)
           tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + s),
-                      c * C::CH, j * C::BN, bh);
+                      c * C::CH, kv_row0, bh);
         issued = j + 1;
       }
       if (*abort_flag) {
         // Let every copy already issued land before the CTA's shared memory goes away.
-        drain_wait(bar(C::B_QFULL), 0);
+        if (npos > 0) drain_wait(bar(C::B_QFULL), 0);
         const int nk = issued >= 0 ? issued : -issued;
         const int nv = issued >= 0 ? issued : -issued - 1;
         for (int s = 0; s < C::NST; ++s) {
@@ -213,45 +254,56 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
     } else if (warp == 9 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
-      // Each query tile runs its own chain S(0), PV(0), S(1), PV(1), ...; the
-      // issuer polls both chains and issues whichever next MMA group is ready,
-      // so one tile's softmax never holds up the other tile's MMAs.
-      //   S_q(j)  needs K_j resident and PV_q(j-1) complete (P_q aliases S_q);
-      //   PV_q(j) needs V_j resident and P_q(j) written by the softmax.
-      // A K (V) stage is released once both tiles have issued their S (PV) on it.
+      // Each query tile runs its own chain S, PV, S, PV, ... over the positions
+      // it uses; the issuer polls both chains and issues whichever next MMA
+      // group is ready, so one tile's softmax never holds up the other's MMAs.
+      //   S_q at position p  needs K_p resident and the tile's previous PV
+      //                      complete (P_q aliases S_q);
+      //   PV_q at position p needs V_p resident and P_q written by the softmax.
+      // A K (V) stage is released once both tiles are past its position.
       const uint32_t idesc_s = instr_desc_f16(C::BM, C::BN, BF16, false, false, negate != 0);
       const uint32_t idesc_o = instr_desc_f16(C::BM, D, BF16, false, true);
-      bool ok = nkv_max == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
+      bool ok = npos == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
       tc_fence_after_sync();
-      int js[2] = {0, 0};  // next S index per tile
-      int jp[2] = {0, 0};  // next PV index per tile
-      int k_rel = 0, v_rel = 0;  // next key/value tile whose stage is still held
+      int sp[2] = {0, 0};  // next position to consider for S, per tile
+      int pp[2] = {0, 0};  // next position to consider for PV, per tile
+      int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
+      int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
+      int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
       uint64_t t_idle = global_timer_ns();
-      while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
+      while (ok && (k_rel < npos || v_rel < npos)) {
         bool progress = false;
+        // Loads are observed strictly in position order: when position p is
+        // probed, every earlier load on its stage has been seen, so the stage
+        // barrier is at most one phase ahead and the parity test is exact.  (A
+        // tile that skips positions must not probe a later phase directly.)
+        while (k_ready < npos && mbar_probe(bar(C::B_KFULL + k_ready % C::NST), (k_ready / C::NST) & 1))
+          ++k_ready;
+        while (v_ready < npos && mbar_probe(bar(C::B_VFULL + v_ready % C::NST), (v_ready / C::NST) & 1))
+          ++v_ready;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-          // PV_q(jp)
-          const int jv = jp[q];
-          if (jv < nkv[q] && jv < js[q] &&
-              mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
-              mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
+          while (sp[q] < npos && !uses(q, sp[q])) ++sp[q];
+          while (pp[q] < sp[q] && !uses(q, pp[q])) ++pp[q];
+          // PV_q at pp (its S was issued: every used position below sp has one)
+          const int jv = pp[q];
+          if (jv < sp[q] && jv < v_ready && mbar_probe(bar(C::B_PFULL + q), np[q] & 1)) {
             tc_fence_after_sync();
             const uint32_t d_o = tmem + 2 * C::BN + q * D;
             const uint32_t a_p = tmem + q * C::BN;
             const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
 #pragma unroll
             for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+              mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (np[q] > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar(C::B_ODONE + q));
-            jp[q] = jv + 1;
+            pp[q] = jv + 1;
+            ++np[q];
             progress = true;
           }
-          // S_q(js)
-          const int jk = js[q];
-          if (jk < nkv[q] && jk == jp[q] &&
-              mbar_probe(bar(C::B_KFULL + jk % C::NST), (jk / C::NST) & 1) &&
-              (jk == 0 || mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1))) {
+          // S_q at sp
+          const int jk = sp[q];
+          if (jk < npos && ns[q] == np[q] && jk < k_ready &&
+              (ns[q] == 0 || mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1))) {
             tc_fence_after_sync();
             const uint32_t d_s = tmem + q * C::BN;
             const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
@@ -260,16 +312,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
                      kk > 0 ? 1u : 0u);
             tc_commit(bar(C::B_SFULL + q));
-            js[q] = jk + 1;
+            sp[q] = jk + 1;
+            ++ns[q];
             progress = true;
           }
         }
-        // release stages both tiles are done issuing from
-        while (k_rel < nkv_max && (js[0] > k_rel || k_rel >= nkv[0]) && (js[1] > k_rel || k_rel >= nkv[1])) {
+        // release stages both tiles are past
+        while (k_rel < npos && sp[0] > k_rel && sp[1] > k_rel) {
           tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
           ++k_rel;
         }
-        while (v_rel < nkv_max && (jp[0] > v_rel || v_rel >= nkv[0]) && (jp[1] > v_rel || v_rel >= nkv[1])) {
+        while (v_rel < npos && pp[0] > v_rel && pp[1] > v_rel) {
           tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
           ++v_rel;
         }
@@ -305,7 +358,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     float l_exact = 0.f;   // sum of exp2(t - m) in fp32: gives LSE
     float l_round = 0.f;   // sum of the rounded P values: normalises O
     bool ok = true;
-    const int nk = nkv[q];
+    const int nk = cnt[q];
+    int pos = 0;  // position of this tile's next key tile
     const float2 sl2x2 = make_float2(sl2, sl2);
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
@@ -320,7 +374,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[64 + c] = __uint_as_float(u[c]);
       }
-      const int kv0 = j * C::BN;
+      while (!uses(q, pos)) ++pos;
+      const int kv0 = kv_tile(pos++) * C::BN;
       const bool masked = (kv0 + C::BN > N) || (causal && kv0 + C::BN - 1 > row0);
       int lim = C::BN;  // keys kv0 + c with c < lim are visible to this row
       if (masked) {
@@ -422,6 +477,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
       if (row < N) lse_out[static_cast<int64_t>(bh) * N + row] = (m + log2f(l_exact)) * 0.69314718055994531f;
+    } else if (SPARSE && ok && nk == 0 && row < N) {
+      // the mask hides every key from this row: O = 0, LSE = -inf
+      uint4* dst = reinterpret_cast<uint4*>(o_out + (static_cast<int64_t>(bh) * N + row) * (D * 2));
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+      lse_out[static_cast<int64_t>(bh) * N + row] = -INFINITY;
     }
   }
 
@@ -433,7 +494,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPARSE>
 int launch_fwd_t(const FwdArgs& a) {
   using C = FwdCfg<D>;
   CUtensorMap mq, mk, mv;
@@ -442,23 +503,33 @@ int launch_fwd_t(const FwdArgs& a) {
       !encode_bhnd_map(&mk, a.k, a.BH, a.N, D, C::CH, 128, rowb, BF16) ||
       !encode_bhnd_map(&mv, a.v, a.BH, a.N, D, C::CH, 128, rowb, BF16))
     return kStatusCuda;
-  auto kern = attn_fwd_kernel<D, BF16>;
+  auto kern = attn_fwd_kernel<D, BF16, SPARSE>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
   // The warpgroup register split adds up only at this launch allocation.
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, static_cast<uint8_t*>(a.o), a.lse,
-                                                      a.N, a.sl2, a.causal, a.negate, a.status);
+                                                      a.N, a.sl2, a.causal, a.negate, a.bmask, a.H,
+                                                      a.mask_heads, a.status);
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }
 
 }  // namespace
 
 int launch_fwd(const FwdArgs& a) {
+  if (a.bmask) {  // block-sparse: bf16 only, at most kMaxSparseTiles key tiles
+    if (!a.bf16 || (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+    switch (a.d) {
+      case 32: return launch_fwd_t<32, true, true>(a);
+      case 64: return launch_fwd_t<64, true, true>(a);
+      case 128: return launch_fwd_t<128, true, true>(a);
+      default: return kStatusUnsupported;
+    }
+  }
   switch (a.d) {
-    case 32: return a.bf16 ? launch_fwd_t<32, true>(a) : launch_fwd_t<32, false>(a);
-    case 64: return a.bf16 ? launch_fwd_t<64, true>(a) : launch_fwd_t<64, false>(a);
-    case 128: return a.bf16 ? launch_fwd_t<128, true>(a) : launch_fwd_t<128, false>(a);
+    case 32: return a.bf16 ? launch_fwd_t<32, true, false>(a) : launch_fwd_t<32, false, false>(a);
+    case 64: return a.bf16 ? launch_fwd_t<64, true, false>(a) : launch_fwd_t<64, false, false>(a);
+    case 128: return a.bf16 ? launch_fwd_t<128, true, false>(a) : launch_fwd_t<128, false, false>(a);
     default: return kStatusUnsupported;
   }
 }

@@ -19,6 +19,9 @@ constexpr int kStatusTimeout = 4;
 constexpr int kStatusArch = 5;
 constexpr int kStatusDeviceCheck = 6;
 
+// Block-sparse forward: at most this many 128-key tiles (N <= 65536).
+constexpr int kMaxSparseTiles = 512;
+
 struct FwdArgs {
   const void *q, *k, *v;
   void* o;
@@ -30,6 +33,10 @@ struct FwdArgs {
   bool bf16;
   cudaStream_t stream;
   int* status;
+  // block-sparse only (nullptr otherwise): [mask_heads][nb][nb] bytes, nb = ceil(N/128)
+  const uint8_t* bmask = nullptr;
+  int H = 1;
+  int mask_heads = 1;
 };
 
 struct BwdArgs {

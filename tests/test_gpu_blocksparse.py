@@ -1,0 +1,116 @@
+"""Block-sparse forward against the float64 oracle with the same block mask
+(key j visible to query i iff mask[h][i//128][j//128] != 0, and j <= i if
+causal; a row seeing no key has O = 0, LSE = -inf).  Tolerances are the
+forward's: max |dO| <= 1e-2 beyond the output type's rounding, max
+|dLSE| <= 1e-3; masked structure must hold exactly."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from io_aware_exact_12_gb300 import build as b
+    b.build()
+    import io_aware_exact_12_gb300 as p
+    p.lib()
+    return p
+
+
+def _half_ulp_bf16(ref):
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 1e-30)))
+    return np.exp2(e - 8)
+
+
+def _random_mask(heads, nb, density, seed, keep_diag=True):
+    g = torch.Generator().manual_seed(seed)
+    m = (torch.rand((heads, nb, nb), generator=g) < density).to(torch.uint8)
+    if keep_diag:
+        m[:, torch.arange(nb), torch.arange(nb)] = 1
+    return m
+
+
+def _check(pkg, shape, mask, causal, seed, scale=None):
+    x = make_inputs(shape, "bf16", seed=seed, with_grad=False)
+    scale = 1.0 / math.sqrt(shape.d) if scale is None else scale
+    o, lse = pkg.attn_fwd_blocksparse(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), mask.cuda(), scale=scale,
+                                      causal=causal)
+    assert pkg.sync_status() == 0
+    f = lambda t: t.double().numpy()  # noqa: E731
+    oo, lo = oracle.forward(f(x["q"]), f(x["k"]), f(x["v"]), scale, causal, block_mask=mask.numpy(), blk=128)
+    go, gl = o.double().cpu().numpy(), lse.double().cpu().numpy()
+    empty = np.isneginf(lo)
+    assert np.array_equal(np.isneginf(gl), empty)            # the same rows see no key
+    assert (go[empty] == 0).all()
+    err = np.abs(go - oo)
+    assert (err - _half_ulp_bf16(oo)).max() <= 1e-2, "max|dO| %g" % err.max()
+    assert np.abs(gl[~empty] - lo[~empty]).max() <= 1e-3
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(1000, 128), (640, 64), (300, 32)])
+def test_random_block_masks(pkg, N, d, causal):
+    nb = (N + 127) // 128
+    _check(pkg, AttnShape(2, 3, N, d), _random_mask(3, nb, 0.4, seed=N + d), causal, seed=N)
+
+
+def test_shared_mask_and_empty_rows(pkg):
+    N, nb = 700, 6
+    mask = _random_mask(1, nb, 0.5, seed=3, keep_diag=False)
+    mask[0, 2, :] = 0  # query block 2 sees nothing
+    mask[0, 0, 0] = 1
+    _check(pkg, AttnShape(1, 4, N, 128), mask, False, seed=5)
+
+
+def test_all_ones_mask_equals_dense_forward_bitwise(pkg):
+    shape = AttnShape(1, 2, 900, 128)
+    x = make_inputs(shape, "bf16", seed=7, with_grad=False)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    mask = torch.ones((1, 8, 8), dtype=torch.uint8, device="cuda")
+    for causal in (False, True):
+        o1, l1 = pkg.attn_fwd(q, k, v, scale=0.1, causal=causal)
+        o2, l2 = pkg.attn_fwd_blocksparse(q, k, v, mask, scale=0.1, causal=causal)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_block_diagonal_mask(pkg):
+    N, nb = 1024, 8
+    mask = torch.eye(nb, dtype=torch.uint8)[None]
+    _check(pkg, AttnShape(1, 2, N, 128), mask, False, seed=9)
+
+
+def test_sparse_long_sequence_sampled_rows(pkg):
+    """N = 8192 with a 25 %-dense mask: sampled rows against the oracle's
+    definition on the visible keys of each row (rows of the masked problem)."""
+    N, nb, d = 8192, 64, 128
+    mask = _random_mask(1, nb, 0.25, seed=11)
+    x = make_inputs(AttnShape(1, 2, N, d), "bf16", seed=13, with_grad=False)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = pkg.attn_fwd_blocksparse(q, k, v, mask.cuda(), scale=1 / math.sqrt(d), causal=False)
+    assert pkg.sync_status() == 0
+    rng = np.random.default_rng(1)
+    for h, i in zip(rng.integers(0, 2, 24), rng.integers(0, N, 24)):
+        cols = np.concatenate([np.arange(j * 128, min(N, j * 128 + 128)) for j in range(nb)
+                               if mask[0, i // 128, j]])
+        qf = x["q"][0, h].double().numpy()
+        kf = x["k"][0, h].double().numpy()[cols]
+        vf = x["v"][0, h].double().numpy()[cols]
+        # the same problem as oracle rows: query i against the visible keys only
+        L = len(cols)
+        qq = np.zeros((1, 1, L, d))
+        qq[0, 0, L - 1] = qf[i]
+        ro, rl, _ = oracle.rows(qq, kf[None, None], vf[None, None], None, 1 / math.sqrt(d), False,
+                                np.array([0]), np.array([L - 1]))
+        go = o[0, h, i].double().cpu().numpy()
+        assert (np.abs(go - ro[0]) - _half_ulp_bf16(ro[0])).max() <= 1e-2
+        assert abs(lse[0, h, i].item() - rl[0]) <= 1e-3
