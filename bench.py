@@ -260,6 +260,40 @@ def measure_fp8(attn, steps, warmup, peaks):
     return res
 
 
+def measure_blocksparse(attn, steps, warmup, peaks, density=0.25):
+    """Block-sparse forward on the bench shape with a seeded random block mask
+    of the given density (diagonal always on).  Credited FLOPs count only the
+    enabled 128 x 128 tile pairs (4 * 128 * 128 * d each)."""
+    import torch
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+    B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
+    nb = N // 128
+    g = torch.Generator().manual_seed(3)
+    mask = (torch.rand((H, nb, nb), generator=g) < density).to(torch.uint8)
+    mask[:, torch.arange(nb), torch.arange(nb)] = 1
+    x = make_inputs(AttnShape(B, H, N, d), "bf16", seed=4, with_grad=False)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    m = mask.cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    for _ in range(max(warmup, 3)):
+        attn.attn_fwd_blocksparse(q, k, v, m, o=o, lse=lse)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        attn.attn_fwd_blocksparse(q, k, v, m, o=o, lse=lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    pairs = int(mask.sum()) * B
+    fl = 4.0 * 128 * 128 * d * pairs
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    return {"workload": "block-sparse forward, B=2 H=16 N=8192 d=128 bf16, per-head random mask",
+            "density": pairs / (B * H * nb * nb), "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
+            "frac": fl / (ms * 1e-3) / 1e12 / peak, "status": attn.sync_status()}
+
+
 def cpu_model():
     try:
         for ln in open("/proc/cpuinfo"):
@@ -423,6 +457,7 @@ def run_ours(args):
 
     decode = measure_decode(attn, K, args.warmup, peaks) if rank == 0 else None
     fp8 = measure_fp8(attn, K, args.warmup, peaks) if rank == 0 else None
+    sparse = measure_blocksparse(attn, K, args.warmup, peaks) if rank == 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -441,7 +476,7 @@ def run_ours(args):
                 "causal": {"fwd_ms": statistics.median(cf_ms), "bwd_ms": statistics.median(cb_ms),
                            "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
                            "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
-                "roofline": roof, "cpu_baseline": cpu, "decode": decode, "fp8": fp8,
+                "roofline": roof, "cpu_baseline": cpu, "decode": decode, "fp8": fp8, "blocksparse": sparse,
                 "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "gpu_launches_e2e": launches_e2e,

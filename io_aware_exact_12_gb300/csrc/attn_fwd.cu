@@ -261,81 +261,151 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       //                      complete (P_q aliases S_q);
       //   PV_q at position p needs V_p resident and P_q written by the softmax.
       // A K (V) stage is released once both tiles are past its position.
-      const uint32_t idesc_s = instr_desc_f16(C::BM, C::BN, BF16, false, false, negate != 0);
-      const uint32_t idesc_o = instr_desc_f16(C::BM, D, BF16, false, true);
-      bool ok = npos == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
-      tc_fence_after_sync();
-      int sp[2] = {0, 0};  // next position to consider for S, per tile
-      int pp[2] = {0, 0};  // next position to consider for PV, per tile
-      int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
-      int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
-      int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
-      uint64_t t_idle = global_timer_ns();
-      while (ok && (k_rel < npos || v_rel < npos)) {
-        bool progress = false;
-        // Loads are observed strictly in position order: when position p is
-        // probed, every earlier load on its stage has been seen, so the stage
-        // barrier is at most one phase ahead and the parity test is exact.  (A
-        // tile that skips positions must not probe a later phase directly.)
-        while (k_ready < npos && mbar_probe(bar(C::B_KFULL + k_ready % C::NST), (k_ready / C::NST) & 1))
-          ++k_ready;
-        while (v_ready < npos && mbar_probe(bar(C::B_VFULL + v_ready % C::NST), (v_ready / C::NST) & 1))
-          ++v_ready;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          while (sp[q] < npos && !uses(q, sp[q])) ++sp[q];
-          while (pp[q] < sp[q] && !uses(q, pp[q])) ++pp[q];
-          // PV_q at pp (its S was issued: every used position below sp has one)
-          const int jv = pp[q];
-          if (jv < sp[q] && jv < v_ready && mbar_probe(bar(C::B_PFULL + q), np[q] & 1)) {
-            tc_fence_after_sync();
-            const uint32_t d_o = tmem + 2 * C::BN + q * D;
-            const uint32_t a_p = tmem + q * C::BN;
-            const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < C::BN / 16; ++kk)
-              mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (np[q] > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar(C::B_ODONE + q));
-            pp[q] = jv + 1;
-            ++np[q];
-            progress = true;
+      if constexpr (!SPARSE) {
+        const uint32_t idesc_s = instr_desc_f16(C::BM, C::BN, BF16, false, false, negate != 0);
+        const uint32_t idesc_o = instr_desc_f16(C::BM, D, BF16, false, true);
+        bool ok = nkv_max == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
+        tc_fence_after_sync();
+        int js[2] = {0, 0};  // next S index per tile
+        int jp[2] = {0, 0};  // next PV index per tile
+        int k_rel = 0, v_rel = 0;  // next key/value tile whose stage is still held
+        uint64_t t_idle = global_timer_ns();
+        while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
+          bool progress = false;
+  #pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            // PV_q(jp)
+            const int jv = jp[q];
+            if (jv < nkv[q] && jv < js[q] &&
+                mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
+                mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
+              tc_fence_after_sync();
+              const uint32_t d_o = tmem + 2 * C::BN + q * D;
+              const uint32_t a_p = tmem + q * C::BN;
+              const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+  #pragma unroll
+              for (int kk = 0; kk < C::BN / 16; ++kk)
+                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(bar(C::B_ODONE + q));
+              jp[q] = jv + 1;
+              progress = true;
+            }
+            // S_q(js)
+            const int jk = js[q];
+            if (jk < nkv[q] && jk == jp[q] &&
+                mbar_probe(bar(C::B_KFULL + jk % C::NST), (jk / C::NST) & 1) &&
+                (jk == 0 || mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1))) {
+              tc_fence_after_sync();
+              const uint32_t d_s = tmem + q * C::BN;
+              const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
+  #pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
+                       kk > 0 ? 1u : 0u);
+              tc_commit(bar(C::B_SFULL + q));
+              js[q] = jk + 1;
+              progress = true;
+            }
           }
-          // S_q at sp
-          const int jk = sp[q];
-          if (jk < npos && ns[q] == np[q] && jk < k_ready &&
-              (ns[q] == 0 || mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1))) {
-            tc_fence_after_sync();
-            const uint32_t d_s = tmem + q * C::BN;
-            const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-              mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
-                     kk > 0 ? 1u : 0u);
-            tc_commit(bar(C::B_SFULL + q));
-            sp[q] = jk + 1;
-            ++ns[q];
-            progress = true;
+          // release stages both tiles are done issuing from
+          while (k_rel < nkv_max && (js[0] > k_rel || k_rel >= nkv[0]) && (js[1] > k_rel || k_rel >= nkv[1])) {
+            tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
+            ++k_rel;
+          }
+          while (v_rel < nkv_max && (jp[0] > v_rel || v_rel >= nkv[0]) && (jp[1] > v_rel || v_rel >= nkv[1])) {
+            tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
+            ++v_rel;
+          }
+          if (progress) {
+            t_idle = global_timer_ns();
+          } else {
+            if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
+              *abort_flag = 1;
+              ok = false;
+            } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicExch(status, kStatusTimeout);
+              ok = false;
+            }
           }
         }
-        // release stages both tiles are past
-        while (k_rel < npos && sp[0] > k_rel && sp[1] > k_rel) {
-          tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
-          ++k_rel;
-        }
-        while (v_rel < npos && pp[0] > v_rel && pp[1] > v_rel) {
-          tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
-          ++v_rel;
-        }
-        if (progress) {
-          t_idle = global_timer_ns();
-        } else {
-          if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
-            *abort_flag = 1;
-            ok = false;
-          } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicExch(status, kStatusTimeout);
-            ok = false;
+      } else {
+        const uint32_t idesc_s = instr_desc_f16(C::BM, C::BN, BF16, false, false, negate != 0);
+        const uint32_t idesc_o = instr_desc_f16(C::BM, D, BF16, false, true);
+        bool ok = npos == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
+        tc_fence_after_sync();
+        int sp[2] = {0, 0};  // next position to consider for S, per tile
+        int pp[2] = {0, 0};  // next position to consider for PV, per tile
+        int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
+        int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
+        int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
+        uint64_t t_idle = global_timer_ns();
+        while (ok && (k_rel < npos || v_rel < npos)) {
+          bool progress = false;
+          // Loads are observed strictly in position order: when position p is
+          // probed, every earlier load on its stage has been seen, so the stage
+          // barrier is at most one phase ahead and the parity test is exact.  (A
+          // tile that skips positions must not probe a later phase directly.)
+          while (k_ready < npos && mbar_probe(bar(C::B_KFULL + k_ready % C::NST), (k_ready / C::NST) & 1))
+            ++k_ready;
+          while (v_ready < npos && mbar_probe(bar(C::B_VFULL + v_ready % C::NST), (v_ready / C::NST) & 1))
+            ++v_ready;
+  #pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            while (sp[q] < npos && !uses(q, sp[q])) ++sp[q];
+            while (pp[q] < sp[q] && !uses(q, pp[q])) ++pp[q];
+            // PV_q at pp (its S was issued: every used position below sp has one)
+            const int jv = pp[q];
+            if (jv < sp[q] && jv < v_ready && mbar_probe(bar(C::B_PFULL + q), np[q] & 1)) {
+              tc_fence_after_sync();
+              const uint32_t d_o = tmem + 2 * C::BN + q * D;
+              const uint32_t a_p = tmem + q * C::BN;
+              const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+  #pragma unroll
+              for (int kk = 0; kk < C::BN / 16; ++kk)
+                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (np[q] > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(bar(C::B_ODONE + q));
+              pp[q] = jv + 1;
+              ++np[q];
+              progress = true;
+            }
+            // S_q at sp
+            const int jk = sp[q];
+            if (jk < npos && ns[q] == np[q] && jk < k_ready &&
+                (ns[q] == 0 || mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1))) {
+              tc_fence_after_sync();
+              const uint32_t d_s = tmem + q * C::BN;
+              const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
+  #pragma unroll
+              for (int kk = 0; kk < D / 16; ++kk)
+                mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
+                       kk > 0 ? 1u : 0u);
+              tc_commit(bar(C::B_SFULL + q));
+              sp[q] = jk + 1;
+              ++ns[q];
+              progress = true;
+            }
+          }
+          // release stages both tiles are past
+          while (k_rel < npos && sp[0] > k_rel && sp[1] > k_rel) {
+            tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
+            ++k_rel;
+          }
+          while (v_rel < npos && pp[0] > v_rel && pp[1] > v_rel) {
+            tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
+            ++v_rel;
+          }
+          if (progress) {
+            t_idle = global_timer_ns();
+          } else {
+            if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
+              *abort_flag = 1;
+              ok = false;
+            } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicExch(status, kStatusTimeout);
+              ok = false;
+            }
           }
         }
       }
@@ -374,8 +444,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[64 + c] = __uint_as_float(u[c]);
       }
-      while (!uses(q, pos)) ++pos;
-      const int kv0 = kv_tile(pos++) * C::BN;
+      int kv0 = j * C::BN;
+      if constexpr (SPARSE) {
+        while (!uses(q, pos)) ++pos;
+        kv0 = kv_tile(pos++) * C::BN;
+      }
       const bool masked = (kv0 + C::BN > N) || (causal && kv0 + C::BN - 1 > row0);
       int lim = C::BN;  // keys kv0 + c with c < lim are visible to this row
       if (masked) {
