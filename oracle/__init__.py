@@ -54,8 +54,22 @@ def _load():
                                     ctypes.c_int]
         lib.oracle_cols.argtypes = [P, P, P, P, P, P, I64, I64, I64, ctypes.c_double, ctypes.c_int, P, P, I64, P,
                                     P, ctypes.c_int]
+        D, U64, U32 = ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32
+        lib.oracle_philox4x32_10.argtypes = [P, P, P]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_dropout_keep.argtypes = [D, U64, U32, I64, I64, I64, P]
+        lib.oracle_forward_dropout.argtypes = [P, P, P, P, P, P, I64, I64, I64, D, ctypes.c_int, D, U64, U32,
+                                               ctypes.c_int]
+        lib.oracle_backward_dropout.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, D, ctypes.c_int, D, U64,
+                                                U32, ctypes.c_int]
+        lib.oracle_rows_dropout.argtypes = [P, P, P, P, I64, I64, I64, D, ctypes.c_int, D, U64, U32, P, P, I64, P,
+                                            P, P, ctypes.c_int]
+        lib.oracle_cols_dropout.argtypes = [P, P, P, P, P, P, I64, I64, I64, D, ctypes.c_int, D, U64, U32, P, P,
+                                            I64, P, P, ctypes.c_int]
         for f in (lib.oracle_forward, lib.oracle_backward, lib.oracle_rows, lib.oracle_cols,
-                  lib.oracle_forward_masked, lib.oracle_backward_masked):
+                  lib.oracle_forward_masked, lib.oracle_backward_masked, lib.oracle_dropout_keep,
+                  lib.oracle_forward_dropout, lib.oracle_backward_dropout, lib.oracle_rows_dropout,
+                  lib.oracle_cols_dropout):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -92,12 +106,43 @@ def _mask(block_mask, H, N, blk):
     return m, m.shape[0]
 
 
-def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None, blk=128):
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 of a 4-word counter and 2-word key (uint32 each) -> 4 words."""
+    c = (ctypes.c_uint32 * 4)(*[int(x) & 0xFFFFFFFF for x in ctr])
+    kk = (ctypes.c_uint32 * 2)(*[int(x) & 0xFFFFFFFF for x in key])
+    out = (ctypes.c_uint32 * 4)()
+    _load().oracle_philox4x32_10(ctypes.cast(c, ctypes.c_void_p), ctypes.cast(kk, ctypes.c_void_p),
+                                 ctypes.cast(out, ctypes.c_void_p))
+    return [int(x) for x in out]
+
+
+def dropout_keep(p, seed, offset, bh, n_rows, n_cols):
+    """keep_ij in {0, 1} (uint8 [n_rows, n_cols]) of flattened head ``bh``."""
+    out = np.empty((n_rows, n_cols), dtype=np.uint8)
+    rc = _load().oracle_dropout_keep(float(p), int(seed), int(offset), int(bh), n_rows, n_cols, _ptr(out))
+    if rc:
+        raise RuntimeError("oracle_dropout_keep failed (%d)" % rc)
+    return out
+
+
+def _drop(dropout, block_mask):
+    """dropout = (p, seed, offset) or None."""
+    if dropout is None:
+        return None
+    if block_mask is not None:
+        raise ValueError("dropout and block_mask are not combined")
+    p, seed, offset = dropout
+    return float(p), int(seed), int(offset)
+
+
+def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None, blk=128, dropout=None):
     """O, LSE (and optionally P) of softmax(scale q k^T [+ causal mask]) v.
 
     q, k, v: [B, H, N, d] (any float dtype; upcast exactly to float64).
     block_mask: optional [H or 1, nb, nb] (nb = ceil(N/blk)); key j is hidden
     from query i unless block_mask[h][i // blk][j // blk] is nonzero.
+    dropout: optional (p, seed, offset): inverted dropout on P (P returned
+    by want_p is the softmax before dropout; LSE is undropped).
     Returns (o [B,H,N,d], lse [B,H,N]) or (o, lse, p [B,H,N,N]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -106,7 +151,11 @@ def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None,
     lse = np.empty((B, H, N), dtype=np.float64)
     p = np.empty((B, H, N, N), dtype=np.float64) if want_p else None
     m, mh = _mask(block_mask, H, N, blk)
-    if m is None:
+    dr = _drop(dropout, block_mask)
+    if dr is not None:
+        rc = _load().oracle_forward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H, N, d,
+                                            float(scale), int(bool(causal)), *dr, threads or default_threads())
+    elif m is None:
         rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H, N, d,
                                     float(scale), int(bool(causal)), threads or default_threads())
     else:
@@ -118,13 +167,19 @@ def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None,
     return (o, lse, p) if want_p else (o, lse)
 
 
-def backward(q, k, v, o, do, scale, causal, threads=None, block_mask=None, blk=128):
-    """dQ, dK, dV of L = <O, dO>; ``o`` is the oracle's own forward output."""
+def backward(q, k, v, o, do, scale, causal, threads=None, block_mask=None, blk=128, dropout=None):
+    """dQ, dK, dV of L = <O, dO>; ``o`` is the oracle's own forward output
+    (with the same ``dropout``, when given)."""
     q, k, v, o, do = (_f64(x) for x in (q, k, v, o, do))
     B, H, N, d = _shape(q)
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
     m, mh = _mask(block_mask, H, N, blk)
-    if m is None:
+    dr = _drop(dropout, block_mask)
+    if dr is not None:
+        rc = _load().oracle_backward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq), _ptr(dk),
+                                             _ptr(dv), B * H, N, d, float(scale), int(bool(causal)), *dr,
+                                             threads or default_threads())
+    elif m is None:
         rc = _load().oracle_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
                                      B * H, N, d, float(scale), int(bool(causal)), threads or default_threads())
     else:
@@ -136,7 +191,7 @@ def backward(q, k, v, o, do, scale, causal, threads=None, block_mask=None, blk=1
     return dq, dk, dv
 
 
-def rows(q, k, v, do, scale, causal, bh_idx, row_idx, threads=None):
+def rows(q, k, v, do, scale, causal, bh_idx, row_idx, threads=None, dropout=None):
     """O rows, LSE and dQ rows for selected (flattened head, query row) pairs.
 
     Returns (o [n, d], lse [n], dq [n, d] or None when ``do`` is None).
@@ -150,14 +205,20 @@ def rows(q, k, v, do, scale, causal, bh_idx, row_idx, threads=None):
     o = np.empty((n, d), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     dq = np.empty((n, d), dtype=np.float64) if do is not None else None
-    rc = _load().oracle_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, float(scale), int(bool(causal)),
-                             _ptr(bh), _ptr(ri), n, _ptr(o), _ptr(lse), _ptr(dq), threads or default_threads())
+    dr = _drop(dropout, None)
+    if dr is not None:
+        rc = _load().oracle_rows_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, float(scale),
+                                         int(bool(causal)), *dr, _ptr(bh), _ptr(ri), n, _ptr(o), _ptr(lse), _ptr(dq),
+                                         threads or default_threads())
+    else:
+        rc = _load().oracle_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, float(scale), int(bool(causal)),
+                                 _ptr(bh), _ptr(ri), n, _ptr(o), _ptr(lse), _ptr(dq), threads or default_threads())
     if rc:
         raise RuntimeError("oracle_rows failed (%d)" % rc)
     return o, lse, dq
 
 
-def cols(q, k, v, do, lse_all, D_all, scale, causal, bh_idx, col_idx, threads=None):
+def cols(q, k, v, do, lse_all, D_all, scale, causal, bh_idx, col_idx, threads=None, dropout=None):
     """dK, dV rows for selected (flattened head, key) pairs.
 
     lse_all, D_all: [B, H, N] per-row LSE and D_i = sum_k dO_ik O_ik of every row.
@@ -170,9 +231,15 @@ def cols(q, k, v, do, lse_all, D_all, scale, causal, bh_idx, col_idx, threads=No
     n = bh.shape[0]
     dk = np.empty((n, d), dtype=np.float64)
     dv = np.empty((n, d), dtype=np.float64)
-    rc = _load().oracle_cols(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse_all), _ptr(D_all), B * H, N, d,
-                             float(scale), int(bool(causal)), _ptr(bh), _ptr(ci), n, _ptr(dk), _ptr(dv),
-                             threads or default_threads())
+    dr = _drop(dropout, None)
+    if dr is not None:
+        rc = _load().oracle_cols_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse_all), _ptr(D_all), B * H, N,
+                                         d, float(scale), int(bool(causal)), *dr, _ptr(bh), _ptr(ci), n, _ptr(dk),
+                                         _ptr(dv), threads or default_threads())
+    else:
+        rc = _load().oracle_cols(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse_all), _ptr(D_all), B * H, N, d,
+                                 float(scale), int(bool(causal)), _ptr(bh), _ptr(ci), n, _ptr(dk), _ptr(dv),
+                                 threads or default_threads())
     if rc:
         raise RuntimeError("oracle_cols failed (%d)" % rc)
     return dk, dv

@@ -39,6 +39,26 @@
  * key j from query i unless mask[i / blk][j / blk] != 0 (on top of the causal
  * rule).  A row that sees no key at all has O = 0 and LSE = -inf.
  *
+ * Dropout variant (FlashAttention深度攻略 §7, operator fusion: the softmax
+ * step of the fused kernel also applies dropout).  The pages name the step
+ * and nothing more, so the usual inverted dropout on the attention
+ * probabilities is taken:
+ *
+ *   O_i   = sum_j  keep_ij * (256 / t) * P_ij * V_j       (P undropped softmax)
+ *   LSE_i = log sum_j exp(S_ij)                           (statistics undropped)
+ *   dV_j  = sum_i  keep_ij * (256 / t) * P_ij * dO_i
+ *   dP_ij = keep_ij * (256 / t) * dO_i . V_j,   D_i = dO_i . O_i,
+ *   dS    = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ * keep_ij is 1 iff the byte u_ij < t, where t = floor((1 - p) * 256 + 0.5)
+ * (the keep probability rounded to a multiple of 1/256, 1 <= t <= 256) and
+ * u_ij is byte (j mod 4) of word floor((j mod 16) / 4) of
+ *   Philox4x32-10(counter = (floor(j / 16), i, bh, offset), key = (seed lo, seed hi))
+ * -- the counter-based generator of Salmon, Moraes, Dror and Shaw, "Parallel
+ * Random Numbers: As Easy as 1, 2, 3" (SC'11): ten rounds of two 32x32->64
+ * bit multiplies with a Weyl-sequence key schedule.  One call yields the
+ * bytes of 16 consecutive keys of one query row.
+ *
  * Work is spread over threads by (head, block of rows) or (head, block of key
  * columns); each row or column is computed exactly as the definition reads,
  * so threading changes no arithmetic.
@@ -51,6 +71,86 @@
 
 #define ROWS_PER_ITEM 16
 
+/* ---------------------------------------------------------------- Philox */
+
+/* Philox4x32 with 10 rounds (Salmon et al., SC'11): each round multiplies
+ * words 0 and 2 by the two round multipliers, takes the high halves XORed
+ * with the other two words and the round key, and permutes; the key advances
+ * by the Weyl constants (golden ratio and sqrt(3) - 1, as 32-bit fractions)
+ * between rounds. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+  uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint64_t p0 = (uint64_t)0xD2511F53u * x0;
+    const uint64_t p1 = (uint64_t)0xCD9E8D57u * x2;
+    const uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    const uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    const uint32_t y0 = hi1 ^ x1 ^ k0, y2 = hi0 ^ x3 ^ k1;
+    x0 = y0;
+    x1 = lo1;
+    x2 = y2;
+    x3 = lo0;
+  }
+  out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* Dropout parameters: on = 0 disables dropout entirely. */
+typedef struct {
+  int on;
+  uint32_t t;      /* keep iff byte < t, 1 <= t <= 256 */
+  uint32_t key[2]; /* seed, low and high words */
+  uint32_t offset;
+  double rscale;   /* 256 / t */
+} drop_t;
+
+/* The dropout byte u_ij of head bh. */
+static uint32_t drop_byte(const drop_t *dr, int64_t bh, int64_t i, int64_t j) {
+  const uint32_t ctr[4] = {(uint32_t)(j >> 4), (uint32_t)i, (uint32_t)bh, dr->offset};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, dr->key, out);
+  return (out[(j & 15) >> 2] >> (8 * (j & 3))) & 0xFFu;
+}
+
+/* Weight the dropout gives P_ij: 0 (dropped), 256 / t (kept), 1 without dropout. */
+static double drop_weight(const drop_t *dr, int64_t bh, int64_t i, int64_t j) {
+  if (!dr->on) return 1.0;
+  return drop_byte(dr, bh, i, j) < dr->t ? dr->rscale : 0.0;
+}
+
+/* p in [0, 1) -> keep threshold t in [1, 256]; 0 when p is out of range. */
+static uint32_t drop_threshold(double p) {
+  if (!(p >= 0.0 && p < 1.0)) return 0;
+  const double t = floor((1.0 - p) * 256.0 + 0.5);
+  return t < 1.0 ? 0u : (uint32_t)t;
+}
+
+static int drop_init(drop_t *dr, double p, uint64_t seed, uint32_t offset) {
+  memset(dr, 0, sizeof *dr);
+  dr->t = drop_threshold(p);
+  if (dr->t == 0) return 1;
+  dr->on = 1;
+  dr->key[0] = (uint32_t)seed;
+  dr->key[1] = (uint32_t)(seed >> 32);
+  dr->offset = offset;
+  dr->rscale = 256.0 / (double)dr->t;
+  return 0;
+}
+
+/* keep_ij (0/1) of head bh for rows [0, n_rows) and keys [0, n_cols): out[n_rows][n_cols]. */
+int oracle_dropout_keep(double p, uint64_t seed, uint32_t offset, int64_t bh, int64_t n_rows,
+                        int64_t n_cols, uint8_t *out) {
+  drop_t dr;
+  if (drop_init(&dr, p, seed, offset) || n_rows < 0 || n_cols < 0 || !out) return 1;
+  for (int64_t i = 0; i < n_rows; ++i)
+    for (int64_t j = 0; j < n_cols; ++j) out[i * n_cols + j] = drop_byte(&dr, bh, i, j) < dr.t;
+  return 0;
+}
+
 typedef struct {
   const double *q, *k, *v, *o, *dO, *lse, *Dvec;
   double *o_out, *lse_out, *p_out, *dq, *dk, *dv;
@@ -58,6 +158,7 @@ typedef struct {
   int64_t BH, N, d;
   double scale;
   int causal;
+  drop_t drop;
   /* optional block mask */
   const uint8_t *bmask;
   int64_t mask_heads, nb, blk;
@@ -112,11 +213,13 @@ static vis_t vis_for(const job_t *J, int64_t h, int64_t i) {
   return v;
 }
 
-/* One query row of one head, materialising its row of S and P.
- * s_row, p_row: scratch of length N.  Writes o_row[d], *lse_out, and p_row. */
+/* One query row of head h, materialising its row of S and P.
+ * s_row, p_row: scratch of length N.  Writes o_row[d], *lse_out, and p_row
+ * (the softmax probabilities before dropout). */
 static void forward_row(const double *qh, const double *kh, const double *vh, int64_t N,
-                        int64_t d, double scale, vis_t vis, int64_t i, double *s_row,
-                        double *p_row, double *o_row, double *lse_out) {
+                        int64_t d, double scale, vis_t vis, const drop_t *dr, int64_t h,
+                        int64_t i, double *s_row, double *p_row, double *o_row,
+                        double *lse_out) {
   const double *qi = qh + i * d;
   double m = -INFINITY;
   for (int64_t j = 0; j < N; ++j) {
@@ -145,8 +248,10 @@ static void forward_row(const double *qh, const double *kh, const double *vh, in
   for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
   for (int64_t j = 0; j < N; ++j) {
     if (p_row[j] == 0.0) continue;
+    const double w = p_row[j] * drop_weight(dr, h, i, j);
+    if (w == 0.0) continue;
     const double *vj = vh + j * d;
-    for (int64_t c = 0; c < d; ++c) o_row[c] += p_row[j] * vj[c];
+    for (int64_t c = 0; c < d; ++c) o_row[c] += w * vj[c];
   }
   *lse_out = m + log(l);
 }
@@ -164,7 +269,7 @@ static void *fwd_worker(void *arg) {
     const double *qh = J->q + h * N * d, *kh = J->k + h * N * d, *vh = J->v + h * N * d;
     for (int64_t i = rb * ROWS_PER_ITEM; i < N && i < (rb + 1) * ROWS_PER_ITEM; ++i) {
       double *p_row = J->p_out ? J->p_out + (h * N + i) * N : p_tmp;
-      forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), i, s_row, p_row,
+      forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), &J->drop, h, i, s_row, p_row,
                   J->o_out + (h * N + i) * d, J->lse_out + h * N + i);
     }
   }
@@ -175,14 +280,15 @@ static void *fwd_worker(void *arg) {
 
 /* O = softmax(scale Q K^T [+ causal mask]) V and LSE for all heads.
  * p_out: optional [BH][N][N] probabilities (NULL to skip). */
-int oracle_forward_masked(const double *q, const double *k, const double *v, double *o,
-                          double *lse, double *p_out, int64_t BH, int64_t N, int64_t d,
-                          double scale, int causal, const uint8_t *bmask, int64_t mask_heads,
-                          int64_t blk, int nthreads) {
+static int forward_job(const double *q, const double *k, const double *v, double *o, double *lse,
+                       double *p_out, int64_t BH, int64_t N, int64_t d, double scale, int causal,
+                       const uint8_t *bmask, int64_t mask_heads, int64_t blk, const drop_t *dr,
+                       int nthreads) {
   if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !lse) return 1;
   if (bmask && (mask_heads < 1 || blk < 1)) return 1;
   job_t J;
   memset(&J, 0, sizeof J);
+  if (dr) J.drop = *dr;
   J.bmask = bmask; J.mask_heads = mask_heads; J.blk = blk > 0 ? blk : 1;
   J.nb = (N + J.blk - 1) / J.blk;
   J.q = q; J.k = k; J.v = v; J.o_out = o; J.lse_out = lse; J.p_out = p_out;
@@ -192,6 +298,24 @@ int oracle_forward_masked(const double *q, const double *k, const double *v, dou
   run_threads(fwd_worker, &J, nthreads);
   pthread_mutex_destroy(&J.mu);
   return 0;
+}
+
+int oracle_forward_masked(const double *q, const double *k, const double *v, double *o,
+                          double *lse, double *p_out, int64_t BH, int64_t N, int64_t d,
+                          double scale, int causal, const uint8_t *bmask, int64_t mask_heads,
+                          int64_t blk, int nthreads) {
+  return forward_job(q, k, v, o, lse, p_out, BH, N, d, scale, causal, bmask, mask_heads, blk,
+                     NULL, nthreads);
+}
+
+/* Forward with dropout of probability p (p_out, if given, holds P before dropout). */
+int oracle_forward_dropout(const double *q, const double *k, const double *v, double *o,
+                           double *lse, double *p_out, int64_t BH, int64_t N, int64_t d,
+                           double scale, int causal, double p, uint64_t seed, uint32_t offset,
+                           int nthreads) {
+  drop_t dr;
+  if (drop_init(&dr, p, seed, offset)) return 1;
+  return forward_job(q, k, v, o, lse, p_out, BH, N, d, scale, causal, NULL, 0, 0, &dr, nthreads);
 }
 
 int oracle_forward(const double *q, const double *k, const double *v, double *o, double *lse,
@@ -215,16 +339,19 @@ static void *bwd_rows_worker(void *arg) {
     for (int64_t i = it * ROWS_PER_ITEM; i < N && i < (it + 1) * ROWS_PER_ITEM; ++i) {
       double *p_row = J->P_head + i * N, *ds_row = J->dS_head + i * N;
       double lse_unused;
-      forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), i, s_row, p_row, o_row, &lse_unused);
+      forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), &J->drop, h, i, s_row, p_row,
+                  o_row, &lse_unused);
       const double *doi = doh + i * d, *oi = oh + i * d;
       double Di = 0.0;
       for (int64_t c = 0; c < d; ++c) Di += doi[c] * oi[c];
       for (int64_t j = 0; j < N; ++j) {
         if (p_row[j] == 0.0) { ds_row[j] = 0.0; continue; }
+        const double w = drop_weight(&J->drop, h, i, j);
         const double *vj = vh + j * d;
         double dp = 0.0;
         for (int64_t c = 0; c < d; ++c) dp += doi[c] * vj[c];
-        ds_row[j] = p_row[j] * (dp - Di);
+        ds_row[j] = p_row[j] * (w * dp - Di);
+        p_row[j] *= w; /* the weight dV sees */
       }
       double *dqi = J->dq + (h * N + i) * d;
       for (int64_t c = 0; c < d; ++c) dqi[c] = 0.0;
@@ -241,7 +368,8 @@ static void *bwd_rows_worker(void *arg) {
   return NULL;
 }
 
-/* Phase 2 (key columns of one head): dV_j = sum_i P_ij dO_i, dK_j = scale sum_i dS_ij Q_i. */
+/* Phase 2 (key columns of one head): dV_j = sum_i P_ij dO_i (P after dropout),
+ * dK_j = scale sum_i dS_ij Q_i. */
 static void *bwd_cols_worker(void *arg) {
   job_t *J = (job_t *)arg;
   const int64_t N = J->N, d = J->d, h = J->head;
@@ -267,14 +395,15 @@ static void *bwd_cols_worker(void *arg) {
 /* Analytic backward.  o must be the forward output of the same inputs (the
  * oracle's own float64 O).  Materialises P and dS one head at a time
  * (2 * N * N doubles). */
-int oracle_backward_masked(const double *q, const double *k, const double *v, const double *o,
-                           const double *dO, double *dq, double *dk, double *dv, int64_t BH,
-                           int64_t N, int64_t d, double scale, int causal, const uint8_t *bmask,
-                           int64_t mask_heads, int64_t blk, int nthreads) {
+static int backward_job(const double *q, const double *k, const double *v, const double *o,
+                        const double *dO, double *dq, double *dk, double *dv, int64_t BH,
+                        int64_t N, int64_t d, double scale, int causal, const uint8_t *bmask,
+                        int64_t mask_heads, int64_t blk, const drop_t *dr, int nthreads) {
   if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !o || !dO || !dq || !dk || !dv) return 1;
   if (bmask && (mask_heads < 1 || blk < 1)) return 1;
   job_t J;
   memset(&J, 0, sizeof J);
+  if (dr) J.drop = *dr;
   J.bmask = bmask; J.mask_heads = mask_heads; J.blk = blk > 0 ? blk : 1;
   J.nb = (N + J.blk - 1) / J.blk;
   J.q = q; J.k = k; J.v = v; J.o = o; J.dO = dO; J.dq = dq; J.dk = dk; J.dv = dv;
@@ -295,6 +424,26 @@ int oracle_backward_masked(const double *q, const double *k, const double *v, co
   free(J.P_head);
   free(J.dS_head);
   return 0;
+}
+
+int oracle_backward_masked(const double *q, const double *k, const double *v, const double *o,
+                           const double *dO, double *dq, double *dk, double *dv, int64_t BH,
+                           int64_t N, int64_t d, double scale, int causal, const uint8_t *bmask,
+                           int64_t mask_heads, int64_t blk, int nthreads) {
+  return backward_job(q, k, v, o, dO, dq, dk, dv, BH, N, d, scale, causal, bmask, mask_heads, blk,
+                      NULL, nthreads);
+}
+
+/* Backward with dropout; o must be the dropout forward's output for the same
+ * p, seed and offset. */
+int oracle_backward_dropout(const double *q, const double *k, const double *v, const double *o,
+                            const double *dO, double *dq, double *dk, double *dv, int64_t BH,
+                            int64_t N, int64_t d, double scale, int causal, double p,
+                            uint64_t seed, uint32_t offset, int nthreads) {
+  drop_t dr;
+  if (drop_init(&dr, p, seed, offset)) return 1;
+  return backward_job(q, k, v, o, dO, dq, dk, dv, BH, N, d, scale, causal, NULL, 0, 0, &dr,
+                      nthreads);
 }
 
 int oracle_backward(const double *q, const double *k, const double *v, const double *o,
@@ -319,7 +468,8 @@ static void *rows_worker(void *arg) {
     const int64_t h = J->bh_idx[r], i = J->idx[r];
     const double *qh = J->q + h * N * d, *kh = J->k + h * N * d, *vh = J->v + h * N * d;
     double *oi = J->o_out + r * d;
-    forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), i, s_row, p_row, oi, J->lse_out + r);
+    forward_row(qh, kh, vh, N, d, J->scale, vis_for(J, h, i), &J->drop, h, i, s_row, p_row, oi,
+                J->lse_out + r);
     if (!J->dq) continue;
     const double *doi = J->dO + (h * N + i) * d;
     double Di = 0.0;
@@ -331,7 +481,7 @@ static void *rows_worker(void *arg) {
       const double *vj = vh + j * d, *kj = kh + j * d;
       double dp = 0.0;
       for (int64_t c = 0; c < d; ++c) dp += doi[c] * vj[c];
-      const double ds = p_row[j] * (dp - Di);
+      const double ds = p_row[j] * (drop_weight(&J->drop, h, i, j) * dp - Di);
       for (int64_t c = 0; c < d; ++c) dqi[c] += ds * kj[c];
     }
     for (int64_t c = 0; c < d; ++c) dqi[c] *= J->scale;
@@ -341,10 +491,10 @@ static void *rows_worker(void *arg) {
   return NULL;
 }
 
-int oracle_rows(const double *q, const double *k, const double *v, const double *dO,
-                int64_t BH, int64_t N, int64_t d, double scale, int causal,
-                const int64_t *bh_idx, const int64_t *row_idx, int64_t nsel, double *o_rows,
-                double *lse_rows, double *dq_rows, int nthreads) {
+static int rows_job(const double *q, const double *k, const double *v, const double *dO,
+                    int64_t BH, int64_t N, int64_t d, double scale, int causal,
+                    const int64_t *bh_idx, const int64_t *row_idx, int64_t nsel, double *o_rows,
+                    double *lse_rows, double *dq_rows, const drop_t *dr, int nthreads) {
   if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !bh_idx || !row_idx || !o_rows || !lse_rows)
     return 1;
   if (dq_rows && !dO) return 1;
@@ -352,6 +502,7 @@ int oracle_rows(const double *q, const double *k, const double *v, const double 
     if (bh_idx[r] < 0 || bh_idx[r] >= BH || row_idx[r] < 0 || row_idx[r] >= N) return 1;
   job_t J;
   memset(&J, 0, sizeof J);
+  if (dr) J.drop = *dr;
   J.q = q; J.k = k; J.v = v; J.dO = dO; J.o_out = o_rows; J.lse_out = lse_rows; J.dq = dq_rows;
   J.BH = BH; J.N = N; J.d = d; J.scale = scale; J.causal = causal;
   J.bh_idx = bh_idx; J.idx = row_idx; J.nsel = nsel; J.nitems = nsel;
@@ -359,6 +510,25 @@ int oracle_rows(const double *q, const double *k, const double *v, const double 
   run_threads(rows_worker, &J, nthreads);
   pthread_mutex_destroy(&J.mu);
   return 0;
+}
+
+int oracle_rows(const double *q, const double *k, const double *v, const double *dO,
+                int64_t BH, int64_t N, int64_t d, double scale, int causal,
+                const int64_t *bh_idx, const int64_t *row_idx, int64_t nsel, double *o_rows,
+                double *lse_rows, double *dq_rows, int nthreads) {
+  return rows_job(q, k, v, dO, BH, N, d, scale, causal, bh_idx, row_idx, nsel, o_rows, lse_rows,
+                  dq_rows, NULL, nthreads);
+}
+
+int oracle_rows_dropout(const double *q, const double *k, const double *v, const double *dO,
+                        int64_t BH, int64_t N, int64_t d, double scale, int causal, double p,
+                        uint64_t seed, uint32_t offset, const int64_t *bh_idx,
+                        const int64_t *row_idx, int64_t nsel, double *o_rows, double *lse_rows,
+                        double *dq_rows, int nthreads) {
+  drop_t dr;
+  if (drop_init(&dr, p, seed, offset)) return 1;
+  return rows_job(q, k, v, dO, BH, N, d, scale, causal, bh_idx, row_idx, nsel, o_rows, lse_rows,
+                  dq_rows, &dr, nthreads);
 }
 
 /* ----------------------------------------------------- sampled key columns */
@@ -382,18 +552,20 @@ static void *cols_worker(void *arg) {
       double acc = 0.0, dp = 0.0;
       for (int64_t c = 0; c < d; ++c) { acc += qi[c] * kj[c]; dp += doi[c] * vj[c]; }
       const double p = exp(J->scale * acc - J->lse[h * N + i]);
-      const double ds = p * (dp - J->Dvec[h * N + i]);
-      for (int64_t c = 0; c < d; ++c) { dvj[c] += p * doi[c]; dkj[c] += ds * qi[c]; }
+      const double w = drop_weight(&J->drop, h, i, j);
+      const double ds = p * (w * dp - J->Dvec[h * N + i]);
+      for (int64_t c = 0; c < d; ++c) { dvj[c] += w * p * doi[c]; dkj[c] += ds * qi[c]; }
     }
     for (int64_t c = 0; c < d; ++c) dkj[c] *= J->scale;
   }
   return NULL;
 }
 
-int oracle_cols(const double *q, const double *k, const double *v, const double *dO,
-                const double *lse_all, const double *D_all, int64_t BH, int64_t N, int64_t d,
-                double scale, int causal, const int64_t *bh_idx, const int64_t *col_idx,
-                int64_t nsel, double *dk_rows, double *dv_rows, int nthreads) {
+static int cols_job(const double *q, const double *k, const double *v, const double *dO,
+                    const double *lse_all, const double *D_all, int64_t BH, int64_t N, int64_t d,
+                    double scale, int causal, const int64_t *bh_idx, const int64_t *col_idx,
+                    int64_t nsel, double *dk_rows, double *dv_rows, const drop_t *dr,
+                    int nthreads) {
   if (BH < 1 || N < 1 || d < 1 || !q || !k || !v || !dO || !lse_all || !D_all || !bh_idx ||
       !col_idx || !dk_rows || !dv_rows)
     return 1;
@@ -401,6 +573,7 @@ int oracle_cols(const double *q, const double *k, const double *v, const double 
     if (bh_idx[r] < 0 || bh_idx[r] >= BH || col_idx[r] < 0 || col_idx[r] >= N) return 1;
   job_t J;
   memset(&J, 0, sizeof J);
+  if (dr) J.drop = *dr;
   J.q = q; J.k = k; J.v = v; J.dO = dO; J.lse = lse_all; J.Dvec = D_all;
   J.dk = dk_rows; J.dv = dv_rows;
   J.BH = BH; J.N = N; J.d = d; J.scale = scale; J.causal = causal;
@@ -409,4 +582,23 @@ int oracle_cols(const double *q, const double *k, const double *v, const double 
   run_threads(cols_worker, &J, nthreads);
   pthread_mutex_destroy(&J.mu);
   return 0;
+}
+
+int oracle_cols(const double *q, const double *k, const double *v, const double *dO,
+                const double *lse_all, const double *D_all, int64_t BH, int64_t N, int64_t d,
+                double scale, int causal, const int64_t *bh_idx, const int64_t *col_idx,
+                int64_t nsel, double *dk_rows, double *dv_rows, int nthreads) {
+  return cols_job(q, k, v, dO, lse_all, D_all, BH, N, d, scale, causal, bh_idx, col_idx, nsel,
+                  dk_rows, dv_rows, NULL, nthreads);
+}
+
+int oracle_cols_dropout(const double *q, const double *k, const double *v, const double *dO,
+                        const double *lse_all, const double *D_all, int64_t BH, int64_t N,
+                        int64_t d, double scale, int causal, double p, uint64_t seed,
+                        uint32_t offset, const int64_t *bh_idx, const int64_t *col_idx,
+                        int64_t nsel, double *dk_rows, double *dv_rows, int nthreads) {
+  drop_t dr;
+  if (drop_init(&dr, p, seed, offset)) return 1;
+  return cols_job(q, k, v, dO, lse_all, D_all, BH, N, d, scale, causal, bh_idx, col_idx, nsel,
+                  dk_rows, dv_rows, &dr, nthreads);
 }
