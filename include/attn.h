@@ -96,6 +96,35 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream);
 
 /*
+ * Forward and backward with dropout fused into the softmax step (bf16;
+ * FlashAttention深度攻略 §7, operator fusion: the softmax step of the fused
+ * kernel also applies dropout).  Inverted dropout on P:
+ *   t = floor((1 - p_drop) * 256 + 0.5) (in double), the keep probability
+ *   rounded to a multiple of 1/256;
+ *   keep_ij = [u_ij < t], u_ij = byte (j mod 4) of word (j mod 16) / 4 of
+ *     Philox4x32-10(counter = (j / 16, i, b * H + h, offset),
+ *                   key = (seed & 0xffffffff, seed >> 32))
+ *     (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *     1, 2, 3", SC'11);
+ *   O_i = (256 / t) sum_j keep_ij P_ij V_j; LSE is that of the undropped P.
+ * The backward draws the same bytes again (nothing is stored) and returns the
+ * gradients of L = <O, dO>: dV = (256/t) (keep o P)^T dO,
+ * dS = P o ((256/t) keep o (dO V^T) - D), D_i = sum_k dO_ik O_ik,
+ * dQ = scale dS K, dK = scale dS^T Q.  Pass the forward's p_drop, seed and
+ * offset.  Other arguments, layouts, scratch and errors are those of
+ * attn_fwd / attn_bwd; in addition ATTN_ERR_INVALID_ARG when p_drop is not in
+ * [0, 1) or t would be 0 (p_drop > 1 - 1/512).  t = 256 (p_drop < 1/512) is
+ * no dropout and runs attn_fwd / attn_bwd.
+ */
+int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, float p_drop,
+                     unsigned long long seed, unsigned int offset, void* stream);
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                     float scale, int causal, float p_drop, unsigned long long seed,
+                     unsigned int offset, void* stream);
+
+/*
  * Block-sparse forward (bf16): attn_fwd where whole 128 x 128 tiles of the
  * score matrix are enabled or skipped by a block mask (FlashAttention深度攻略,
  * 进阶追问 "Sparse FlashAttention"; the tiles skipped are never loaded or

@@ -19,7 +19,7 @@ import os
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -52,6 +52,11 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_f16.argtypes = L.attn_bwd.argtypes
         for f in (L.attn_fwd, L.attn_fwd_f16, L.attn_bwd, L.attn_bwd_f16):
             f.restype = I
+        U64, U32 = ctypes.c_ulonglong, ctypes.c_uint
+        L.attn_fwd_dropout.argtypes = [P, P, P, P, P, I, I, I, I, F, I, F, U64, U32, P]
+        L.attn_fwd_dropout.restype = I
+        L.attn_bwd_dropout.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, U64, U32, P]
+        L.attn_bwd_dropout.restype = I
         L.attn_fwd_blocksparse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, P]
         L.attn_fwd_blocksparse.restype = I
         L.attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, F, I, P]
@@ -145,6 +150,59 @@ def attn_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
                 _stream_handle(stream))
     if rc:
         raise AttnError("attn_bwd", rc)
+    return dq, dk, dv
+
+
+def attn_fwd_dropout(q, k, v, p_drop, seed, offset=0, scale=None, causal=False, o=None, lse=None, stream=None):
+    """attn_fwd with inverted dropout of probability ``p_drop`` on P, the keep
+    decisions drawn in the kernel from Philox4x32-10 keyed by ``seed`` (64-bit)
+    with ``offset`` (32-bit) as the fourth counter word.  bf16 only.
+    Returns (o, lse); lse is that of the undropped softmax."""
+    B, H, N, d = _dims(q)
+    _check("q", q, None, torch.bfloat16)
+    _check("k", k, q, q.dtype)
+    _check("v", v, q, q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("o", o, q, q.dtype)
+    _check("lse", lse, None, torch.float32)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
+                                    N, d, float(scale), int(bool(causal)), float(p_drop),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                                    _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_fwd_dropout", rc)
+    return o, lse
+
+
+def attn_bwd_dropout(q, k, v, o, do, lse, p_drop, seed, offset=0, scale=None, causal=False, dq=None, dk=None,
+                     dv=None, stream=None):
+    """Gradients of attn_fwd_dropout's output (same p_drop, seed, offset): the
+    keep decisions are drawn again, not stored.  Returns (dq, dk, dv)."""
+    B, H, N, d = _dims(q)
+    _check("q", q, None, torch.bfloat16)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(name, t, q, q.dtype)
+    _check("lse", lse, None, torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(name, t, q, q.dtype)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_bwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                                    float(scale), int(bool(causal)), float(p_drop),
+                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                                    _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_bwd_dropout", rc)
     return dq, dk, dv
 
 

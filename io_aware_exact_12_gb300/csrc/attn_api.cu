@@ -164,8 +164,27 @@ BwdScratch bwd_scratch_layout(int BH, int N, int d) {
 
 namespace {
 
+constexpr DropParams kNoDrop = {0u, 0u, 0u, 0u, 1.f};
+
+// Dropout probability -> keep threshold and Philox key.  t = 256 keeps
+// everything, which is no dropout (t = 0 in the result).
+int make_drop(float p, unsigned long long seed, unsigned int offset, DropParams* out) {
+  if (!std::isfinite(p) || p < 0.f || p >= 1.f) return kStatusInvalid;
+  const double t = std::floor((1.0 - static_cast<double>(p)) * 256.0 + 0.5);
+  if (t < 1.0) return kStatusInvalid;
+  *out = kNoDrop;
+  if (t >= 256.0) return kStatusOk;
+  out->t = static_cast<uint32_t>(t);
+  out->k0 = static_cast<uint32_t>(seed);
+  out->k1 = static_cast<uint32_t>(seed >> 32);
+  out->offset = offset;
+  out->rscale = static_cast<float>(256.0 / t);
+  return kStatusOk;
+}
+
 int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-              int N, int d, float scale, int causal, void* stream, bool bf16) {
+              int N, int d, float scale, int causal, void* stream, bool bf16,
+              const DropParams& drop = kNoDrop) {
   if (!q || !k || !v || !o || !lse) return kStatusInvalid;
   int rc = validate_common(B, H, N, d, scale);
   if (rc) return rc;
@@ -190,6 +209,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
   a.bf16 = bf16;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = st;
+  a.drop = drop;
   rc = launch_fwd(a);
   if (rc == kStatusOk) t_last_launches = 1;
   return rc;
@@ -197,7 +217,7 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dO,
               const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-              float scale, int causal, void* stream, bool bf16) {
+              float scale, int causal, void* stream, bool bf16, const DropParams& drop = kNoDrop) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return kStatusInvalid;
   int rc = validate_common(B, H, N, d, scale);
   if (rc) return rc;
@@ -238,6 +258,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   a.ws_dq = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.dq_off);
   a.ws_lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.lse2_off);
   a.ws_d = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.d_off);
+  a.drop = drop;
   rc = launch_bwd(a);
   const cudaError_t fe = cudaFreeAsync(ws, s);
   if (rc == kStatusOk && fe != cudaSuccess) rc = kStatusCuda;
@@ -363,6 +384,25 @@ int fp8_entry(const void* q, const void* k, const void* v, float dq_s, float dk_
 }  // namespace attn
 
 extern "C" {
+
+int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, float p_drop,
+                     unsigned long long seed, unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true, dr);
+}
+
+int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                     float scale, int causal, float p_drop, unsigned long long seed,
+                     unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, true, dr);
+}
 
 int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
                  float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,

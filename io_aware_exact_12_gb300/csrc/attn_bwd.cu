@@ -43,7 +43,13 @@
 //                         dV [256+D,256+2D).
 // Causal: key tile j only visits query tiles i >= j; the diagonal tile is
 // masked elementwise (P^T[key][query] = 0 when key > query).
+// Dropout (DROP): the keep bytes of the forward are drawn again (dropout.cuh):
+// each half warp draws 16 query rows for its 16 keys and transposes them so a
+// thread holds its key's bytes; dropped P^T entries are cleared before the dV
+// product (dV scaled by 256 / t at the end) and dP^T is weighted by
+// keep * 256 / t in dS^T = P^T o (w dP^T - D).
 #include "attn_internal.h"
+#include "dropout.cuh"
 #include "tc_sm103.cuh"
 
 namespace attn {
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(256) attn_dq_convert_kernel(const float* __res
 }
 
 // -------------------------------------------------------------- main pass
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -202,7 +208,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ lse2,
                     const float* __restrict__ dvec, float* __restrict__ dq_acc,
                     uint8_t* __restrict__ dk_out, uint8_t* __restrict__ dv_out, int N, int Npad,
-                    float sl2, float scale, int causal, int negate, int* status) {
+                    float sl2, float scale, int causal, int negate, int* status,
+                    DropParams drop) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -398,7 +405,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     for (int it = 0; it < nq; ++it) {
       const int s = it % C::NSTQ;
       const int q0 = (i0 + it) * C::BM + g * 64;  // first query of this thread's half
-      if (!(ok = mbar_wait(bar(C::B_SFULL), it & 1, abort_flag, status))) break;
+      ok = mbar_wait(bar(C::B_SFULL), it & 1, abort_flag, status);
+      if constexpr (DROP) ok = __all_sync(0xffffffffu, ok);  // the draws below shuffle across the warp
+      if (!ok) break;
       tc_fence_after_sync();
       float p[64];
       {
@@ -423,10 +432,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (c < first) p[c] = 0.f;
       }
+      // keep bytes of this key for queries q0 + 4w .. q0 + 4w + 3 in kw[w]
+      uint32_t kw[16];
+      if constexpr (DROP) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 r4 = philox4x32_10(
+              make_uint4(static_cast<uint32_t>(kv_row >> 4), static_cast<uint32_t>(q0 + 16 * u + (lane & 15)),
+                         static_cast<uint32_t>(bh), drop.offset),
+              drop.k0, drop.k1);
+          uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+          transpose16x16_bytes(w, lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) kw[4 * u + e] = w[e];
+        }
+      }
+      const uint32_t t2 = drop.t * 0x00010001u;
       {
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+        for (int i = 0; i < 32; ++i) {
+          pk[i] = pack2<BF16>(p[2 * i], p[2 * i + 1]);
+          if constexpr (DROP)
+            pk[i] &= ~drop_mask16(drop_lanes(kw[i >> 1], (i & 1) ? kDropSelHi : kDropSelLo, t2));
+        }
         tmem_st32(tmem + lane_off + C::T_S + g * 64, pk);
       }
       tmem_st_wait();
@@ -445,8 +474,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = c0 * 32 + 2 * i;
-          const float2 gd = add2(make_float2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])),
-                                 nd[c / 2]);
+          float2 gd;
+          if constexpr (DROP) {  // w dP - D with w = keep * 256 / t
+            const uint32_t ln = drop_lanes(kw[c >> 2], (i & 1) ? kDropSelHi : kDropSelLo, t2);
+            const uint32_t rs = __float_as_uint(drop.rscale);
+            gd = fma2(make_float2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])),
+                      make_float2(__uint_as_float(rs & ~drop_mask32_first(ln)),
+                                  __uint_as_float(rs & ~drop_mask32_second(ln))),
+                      nd[c / 2]);
+          } else {
+            gd = add2(make_float2(__uint_as_float(dp[2 * i]), __uint_as_float(dp[2 * i + 1])), nd[c / 2]);
+          }
           const float2 ds = mul2(make_float2(p[c], p[c + 1]), gd);
           pk[i] = pack2<BF16>(ds.x, ds.y);
         }
@@ -467,7 +505,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_after_sync();
       const int64_t rbase = (static_cast<int64_t>(bh) * N + kv_row) * (D * 2);
       const uint32_t tcol = tmem + lane_off + (g == 0 ? C::T_DK : C::T_DV);
-      const float mul = g == 0 ? scale : 1.f;
+      const float mul = g == 0 ? scale : (DROP ? drop.rscale : 1.f);
       uint8_t* dst_row = (g == 0 ? dk_out : dv_out) + rbase;
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -533,7 +571,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP = false>
 int launch_bwd_t(const BwdArgs& a) {
   using C = BwdCfg<D>;
   const int Npad = ((a.N + 127) / 128) * 128;
@@ -544,7 +582,7 @@ int launch_bwd_t(const BwdArgs& a) {
       !encode_bhnd_map(&mv, a.v, a.BH, a.N, D, C::CH, 128, C::ROWB, BF16) ||
       !encode_bhnd_map(&mdo, a.dO, a.BH, a.N, D, C::CH, 128, C::ROWB, BF16))
     return kStatusCuda;
-  auto kern = attn_bwd_kernel<D, BF16>;
+  auto kern = attn_bwd_kernel<D, BF16, DROP>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   {
@@ -557,7 +595,7 @@ int launch_bwd_t(const BwdArgs& a) {
   dim3 grid((a.N + C::BN - 1) / C::BN, a.BH);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, mdo, a.ws_lse2, a.ws_d, a.ws_dq, static_cast<uint8_t*>(a.dk),
-      static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status);
+      static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status, a.drop);
   {
     const int64_t groups = static_cast<int64_t>(a.BH) * a.N * D / 8;
     const int blocks = static_cast<int>(std::min<int64_t>((groups + 255) / 256, 152 * 16));
@@ -570,6 +608,15 @@ int launch_bwd_t(const BwdArgs& a) {
 }  // namespace
 
 int launch_bwd(const BwdArgs& a) {
+  if (a.drop.t != 0) {  // dropout: bf16 only
+    if (!a.bf16) return kStatusUnsupported;
+    switch (a.d) {
+      case 32: return launch_bwd_t<32, true, true>(a);
+      case 64: return launch_bwd_t<64, true, true>(a);
+      case 128: return launch_bwd_t<128, true, true>(a);
+      default: return kStatusUnsupported;
+    }
+  }
   switch (a.d) {
     case 32: return a.bf16 ? launch_bwd_t<32, true>(a) : launch_bwd_t<32, false>(a);
     case 64: return a.bf16 ? launch_bwd_t<64, true>(a) : launch_bwd_t<64, false>(a);

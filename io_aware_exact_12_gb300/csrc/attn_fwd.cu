@@ -32,7 +32,12 @@
 //   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied; only the diagonal tile (and the ragged last tile) are masked.
+// Dropout (DROP): after P is rounded and summed into l, each thread draws the
+// keep bytes of its row (one Philox call per 16 keys, dropout.cuh) and clears
+// the dropped halves of the packed P before it goes to TMEM; the epilogue
+// folds 256 / t into 1 / l.  m, l and LSE stay those of the undropped softmax.
 #include "attn_internal.h"
+#include "dropout.cuh"
 #include "tc_sm103.cuh"
 
 namespace attn {
@@ -117,13 +122,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // per-position bit for each query tile.  Producer, MMA issuer and softmax all
 // walk positions, so a K/V tile is loaded once per CTA and each query tile
 // runs its S/PV chain over its own positions only.
-template <int D, bool BF16, bool SPARSE>
+template <int D, bool BF16, bool SPARSE, bool DROP>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, uint8_t* __restrict__ o_out,
                     float* __restrict__ lse_out, int N, float sl2, int causal, int negate,
-                    const uint8_t* __restrict__ bmask, int H, int mask_heads, int* status) {
+                    const uint8_t* __restrict__ bmask, int H, int mask_heads, int* status,
+                    DropParams drop) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -522,6 +528,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             sr1 = add_halves<BF16>(sr1, pk[i + 1]);
           }
         }
+        if constexpr (DROP) {
+          // keys kv0 + 64 c0 + 16 g + (0..15): one draw; word w covers keys 4w..4w+3
+          const uint32_t t2 = drop.t * 0x00010001u;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 r4 = philox4x32_10(
+                make_uint4(static_cast<uint32_t>(kv0 >> 4) + c0 * 4 + g, static_cast<uint32_t>(row),
+                           static_cast<uint32_t>(bh), drop.offset),
+                drop.k0, drop.k1);
+            const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+              pk[8 * g + 2 * w] &= ~drop_mask16(drop_lanes(rw[w], kDropSelLo, t2));
+              pk[8 * g + 2 * w + 1] &= ~drop_mask16(drop_lanes(rw[w], kDropSelHi, t2));
+            }
+          }
+        }
         tmem_st32(tS + c0 * 32, pk);
       }
       l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
@@ -533,7 +556,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     if (ok && nk > 0 && mbar_wait(bar(C::B_ODONE + q), (nk - 1) & 1, abort_flag, status)) {
       tc_fence_after_sync();
-      const float inv_l = 1.0f / l_round;
+      const float inv_l = (DROP ? drop.rscale : 1.0f) / l_round;
       uint8_t* orow = o_out + (static_cast<int64_t>(bh) * N + row) * (D * 2);
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
@@ -567,7 +590,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   }
 }
 
-template <int D, bool BF16, bool SPARSE>
+template <int D, bool BF16, bool SPARSE, bool DROP = false>
 int launch_fwd_t(const FwdArgs& a) {
   using C = FwdCfg<D>;
   CUtensorMap mq, mk, mv;
@@ -576,20 +599,29 @@ int launch_fwd_t(const FwdArgs& a) {
       !encode_bhnd_map(&mk, a.k, a.BH, a.N, D, C::CH, 128, rowb, BF16) ||
       !encode_bhnd_map(&mv, a.v, a.BH, a.N, D, C::CH, 128, rowb, BF16))
     return kStatusCuda;
-  auto kern = attn_fwd_kernel<D, BF16, SPARSE>;
+  auto kern = attn_fwd_kernel<D, BF16, SPARSE, DROP>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
   // The warpgroup register split adds up only at this launch allocation.
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, static_cast<uint8_t*>(a.o), a.lse,
                                                       a.N, a.sl2, a.causal, a.negate, a.bmask, a.H,
-                                                      a.mask_heads, a.status);
+                                                      a.mask_heads, a.status, a.drop);
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }
 
 }  // namespace
 
 int launch_fwd(const FwdArgs& a) {
+  if (a.drop.t != 0) {  // dropout: bf16, dense
+    if (!a.bf16 || a.bmask) return kStatusUnsupported;
+    switch (a.d) {
+      case 32: return launch_fwd_t<32, true, false, true>(a);
+      case 64: return launch_fwd_t<64, true, false, true>(a);
+      case 128: return launch_fwd_t<128, true, false, true>(a);
+      default: return kStatusUnsupported;
+    }
+  }
   if (a.bmask) {  // block-sparse: bf16 only, at most kMaxSparseTiles key tiles
     if (!a.bf16 || (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
     switch (a.d) {

@@ -22,6 +22,16 @@ constexpr int kStatusDeviceCheck = 6;
 // Block-sparse forward: at most this many 128-key tiles (N <= 65536).
 constexpr int kMaxSparseTiles = 512;
 
+// Dropout fused into the softmax step (t == 0: off).  Element (i, j) of head
+// bh is kept iff a Philox byte drawn for it is below t; kept probabilities
+// are scaled by rscale = 256 / t.
+struct DropParams {
+  uint32_t t;          // keep threshold, 1..256
+  uint32_t k0, k1;     // Philox key: seed low / high words
+  uint32_t offset;     // fourth counter word
+  float rscale;
+};
+
 struct FwdArgs {
   const void *q, *k, *v;
   void* o;
@@ -37,6 +47,7 @@ struct FwdArgs {
   const uint8_t* bmask = nullptr;
   int H = 1;
   int mask_heads = 1;
+  DropParams drop = {0u, 0u, 0u, 0u, 1.f};
 };
 
 struct BwdArgs {
@@ -55,6 +66,7 @@ struct BwdArgs {
   float* ws_dq;
   float* ws_lse2;
   float* ws_d;
+  DropParams drop = {0u, 0u, 0u, 0u, 1.f};
 };
 
 // Bytes of backward scratch for a problem, and its carve-up.

@@ -96,3 +96,12 @@ def test_valid_arguments_without_gpu_report_an_error(L):
         pytest.skip("a GPU is present: a call with fake pointers would launch")
     rc = _fwd(L)
     assert rc in (3, 5)  # no CUDA device here: runtime error or wrong architecture, never a launch
+
+
+def test_dropout_rejects_bad_probability(L):
+    args = [FAKE, FAKE + 0x100000, FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, 1, 1, 16, 64, 0.125, 0]
+    for p in (1.0, -0.1, float("nan"), 0.999):
+        assert L.attn_fwd_dropout(*args, p, 1, 0, None) == 1
+    bargs = [FAKE + i * 0x100000 for i in range(9)] + [1, 2, 100, 128, 0.1, 1]
+    assert L.attn_bwd_dropout(*bargs, 1.5, 1, 0, None) == 1
+    assert L.attn_bwd_dropout(*bargs[:9], 1, 2, 100, 96, 0.1, 1, 0.1, 1, 0, None) == 2

@@ -1,0 +1,234 @@
+"""GPU parity of the dropout forward and backward against the float64 oracle.
+
+The keep decisions are integer work and are checked bit-exactly: with Q = 0
+every visible probability is equal, so choosing V (forward) or dO (backward)
+as scaled unit vectors makes each output element an integer count of kept
+entries that can be read back exactly and compared with the oracle's
+keep_ij for every (i, j) of a head.  O, LSE and dQ/dK/dV are compared with
+the tolerances of the plain path (max |dO| <= 1e-2 beyond the output's own
+rounding, max |dLSE| <= 1e-3, relative Frobenius error <= 2e-2), in full on
+small and ragged shapes and on sampled rows and key columns at B=2, H=16,
+N=8192, d=128.
+
+The backward is given O in bf16, so its D_i = sum_k dO_ik O_ik carries the
+rounding of O: |D_kernel - D| <= delta_i = sum_k |dO_ik| ulp(O_ik).  That
+error enters dS_ij as P_ij delta_i, hence dQ_i by up to scale delta_i
+sum_j P_ij |K_j| and dK_j by up to scale sum_i P_ij delta_i |Q_i|.  Without
+dropout O = V exactly at N = 1 and the term vanishes; with dropout it does
+not, and there the exact dQ and dK are zero.  The full comparisons allow this
+term (computed from the oracle's own O and P) on top of the 2e-2 bound.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from io_aware_exact_12_gb300.synth import AttnShape, make_inputs, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_O = 1e-2
+TOL_LSE = 1e-3
+TOL_GRAD = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from io_aware_exact_12_gb300 import build as b
+    b.build()
+    import io_aware_exact_12_gb300 as pkg
+    pkg.lib()
+    yield
+
+
+def _pkg():
+    import io_aware_exact_12_gb300 as pkg
+    return pkg
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def half_ulp_bf16(ref):
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 1e-30)))
+    return np.exp2(e - 8)
+
+
+def rel_fro(a, b, floor=1e-30):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), floor))
+
+
+def threshold(p):
+    return int(math.floor((1.0 - float(np.float32(p))) * 256.0 + 0.5))
+
+
+def run(x, scale, causal, drop):
+    pkg = _pkg()
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    p, seed, off = drop
+    o, lse = pkg.attn_fwd_dropout(q, k, v, p, seed, off, scale=scale, causal=causal)
+    grads = pkg.attn_bwd_dropout(q, k, v, o, do, lse, p, seed, off, scale=scale, causal=causal)
+    assert pkg.sync_status() == 0
+    return o, lse, grads
+
+
+def check_full(x, scale, causal, drop, o, lse, grads):
+    d32 = (float(np.float32(drop[0])), drop[1], drop[2])
+    q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+    oo, lo, P = oracle.forward(q, k, v, scale, causal, want_p=True, dropout=d32)
+    err = np.abs(f64(o) - oo)
+    assert (err - half_ulp_bf16(oo)).max() <= TOL_O, "max|dO| %g" % err.max()
+    assert np.abs(f64(lse) - lo).max() <= TOL_LSE
+    ref = oracle.backward(q, k, v, oo, do, scale, causal, dropout=d32)
+    floor = 1e-3 * float(np.linalg.norm(do))
+    delta = (np.abs(do) * 2 * half_ulp_bf16(oo)).sum(-1)  # [B, H, N]
+    extra = {"dq": abs(scale) * delta[..., None] * (P @ np.abs(k)),
+             "dk": abs(scale) * np.einsum("bhij,bhi,bhic->bhjc", P, delta, np.abs(q)),
+             "dv": np.zeros_like(do)}
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        err = float(np.linalg.norm(f64(g) - r))
+        allowed = TOL_GRAD * max(float(np.linalg.norm(r)), floor) + float(np.linalg.norm(extra[name]))
+        assert err <= allowed, "%s error %g > %g (|ref| %g)" % (name, err, allowed, np.linalg.norm(r))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("p", [0.1, 0.5])
+def test_small_full(causal, p):
+    x = make_inputs(AttnShape(2, 4, 64, 32), "bf16", seed=21)
+    drop = (p, 0x1234_5678_9ABC_DEF0, 3)
+    o, lse, grads = run(x, 1 / math.sqrt(32), causal, drop)
+    check_full(x, 1 / math.sqrt(32), causal, drop, o, lse, grads)
+
+
+@pytest.mark.parametrize("N", [1, 17, 127, 129, 300])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_ragged_full(N, d):
+    x = make_inputs(AttnShape(1, 3, N, d), "bf16", seed=N + d)
+    for causal in (False, True):
+        drop = (0.2, 77 + N, d)
+        o, lse, grads = run(x, 1 / math.sqrt(d), causal, drop)
+        check_full(x, 1 / math.sqrt(d), causal, drop, o, lse, grads)
+
+
+def _decode_counts(val, denom, t):
+    """val = (256/t) * count / denom for integer counts: read the counts back."""
+    c = np.rint(val * denom * t / 256.0)
+    assert np.abs(val * denom * t / 256.0 - c).max() < 0.1
+    return c.astype(np.int64)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_keep_mask_is_bit_exact(causal):
+    """Q = 0, V_j = 2^(j // 128) e_(j mod 128): O_ic counts the kept keys
+    c, c + 128, ... of row i in binary; every keep_ij of 3 heads x 512 x 512."""
+    B, H, N, d = 1, 3, 512, 128
+    p, seed, off = 0.3, 0xDEADBEEF_00C0FFEE, 11
+    t = threshold(p)
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    k = make_inputs(AttnShape(B, H, N, d), "bf16", seed=5)["k"].cuda()
+    j = torch.arange(N)
+    v = torch.zeros(N, d)
+    v[j, j % 128] = torch.exp2((j // 128).float())
+    v = v.expand(B, H, N, d).contiguous().to(torch.bfloat16).cuda()
+    pkg = _pkg()
+    o, lse = pkg.attn_fwd_dropout(q, k, v, p, seed, off, scale=0.1, causal=causal)
+    assert pkg.sync_status() == 0
+    o = f64(o)
+    i = np.arange(N)
+    n_vis = (i + 1) if causal else np.full(N, N)
+    np.testing.assert_allclose(f64(lse)[0], np.log(n_vis)[None, :].repeat(H, 0), atol=1e-5)
+    for h in range(H):
+        cnt = _decode_counts(o[0, h], n_vis[:, None].astype(np.float64), t)  # [N, 128]
+        keep = oracle.dropout_keep(float(np.float32(p)), seed, off, h, N, N).astype(np.int64)
+        if causal:
+            keep = np.tril(keep)
+        want = sum(keep[:, 128 * m:128 * (m + 1)] << m for m in range(4))
+        np.testing.assert_array_equal(cnt, want)
+
+
+def test_backward_keep_mask_is_bit_exact():
+    """Q = 0 (P = 1/N), dO_i = 2^(i // 128) e_(i mod 128): dV_jc counts the
+    kept queries c, c + 128, ... of key j in binary."""
+    B, H, N, d = 1, 2, 512, 128
+    p, seed, off = 0.6, 987654321, 2
+    t = threshold(p)
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    k = make_inputs(AttnShape(B, H, N, d), "bf16", seed=6)["k"].cuda()
+    v = make_inputs(AttnShape(B, H, N, d), "bf16", seed=7)["v"].cuda()
+    i = torch.arange(N)
+    do = torch.zeros(N, d)
+    do[i, i % 128] = torch.exp2((i // 128).float())
+    do = do.expand(B, H, N, d).contiguous().to(torch.bfloat16).cuda()
+    pkg = _pkg()
+    o, lse = pkg.attn_fwd_dropout(q, k, v, p, seed, off, scale=0.1, causal=False)
+    dq, dk, dv = pkg.attn_bwd_dropout(q, k, v, o, do, lse, p, seed, off, scale=0.1, causal=False)
+    assert pkg.sync_status() == 0
+    dv = f64(dv)
+    for h in range(H):
+        cnt = _decode_counts(dv[0, h], float(N), t)  # [N keys, 128]
+        keep = oracle.dropout_keep(float(np.float32(p)), seed, off, h, N, N).astype(np.int64)  # [query, key]
+        kt = keep.T
+        want = sum(kt[:, 128 * m:128 * (m + 1)] << m for m in range(4))
+        np.testing.assert_array_equal(cnt, want)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_sequence_sampled(causal):
+    """B=2 H=16 N=8192 d=128, p = 0.1: sampled rows (O, LSE, dQ) and key columns (dK, dV)."""
+    shape = AttnShape(2, 16, 8192, 128)
+    x = make_inputs(shape, "bf16", seed=4)
+    s = 1 / math.sqrt(128)
+    drop = (0.1, 2024, 7)
+    d32 = (float(np.float32(drop[0])), drop[1], drop[2])
+    o, lse, grads = run(x, s, causal, drop)
+    q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
+    N, d = shape.N, shape.d
+    bh, ri = sample_rows(shape, 256, seed=12)
+    ro, rl, rdq = oracle.rows(q, k, v, do, s, causal, bh, ri, dropout=d32)
+    go = f64(o).reshape(-1, N, d)[bh, ri]
+    err = np.abs(go - ro)
+    assert (err - half_ulp_bf16(ro)).max() <= TOL_O
+    assert np.abs(f64(lse).reshape(-1, N)[bh, ri] - rl).max() <= TOL_LSE
+    assert rel_fro(f64(grads[0]).reshape(-1, N, d)[bh, ri], rdq) <= TOL_GRAD
+    h = 31
+    fo, fl, _ = oracle.rows(q, k, v, None, s, causal, np.full(N, h), np.arange(N), dropout=d32)
+    lse_all = np.zeros((shape.B * shape.H, N))
+    D_all = np.zeros_like(lse_all)
+    lse_all[h] = fl
+    D_all[h] = (do.reshape(-1, N, d)[h] * fo).sum(-1)
+    cols = np.random.default_rng(3).choice(N, size=48, replace=False)
+    cols[:2] = [0, N - 1]
+    dk_ref, dv_ref = oracle.cols(q, k, v, do, lse_all.reshape(2, 16, N), D_all.reshape(2, 16, N), s, causal,
+                                 np.full(48, h), cols, dropout=d32)
+    assert rel_fro(f64(grads[1]).reshape(-1, N, d)[h, cols], dk_ref) <= TOL_GRAD
+    assert rel_fro(f64(grads[2]).reshape(-1, N, d)[h, cols], dv_ref) <= TOL_GRAD
+
+
+def test_tiny_probability_is_the_plain_path_and_draws_are_reproducible():
+    pkg = _pkg()
+    x = make_inputs(AttnShape(1, 2, 200, 64), "bf16", seed=8)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o0, l0 = pkg.attn_fwd(q, k, v, scale=0.125)
+    o1, l1 = pkg.attn_fwd_dropout(q, k, v, 0.001, 5, 0, scale=0.125)  # t = 256: nothing dropped
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    a, _ = pkg.attn_fwd_dropout(q, k, v, 0.25, 5, 0, scale=0.125)
+    b, _ = pkg.attn_fwd_dropout(q, k, v, 0.25, 5, 0, scale=0.125)
+    c, _ = pkg.attn_fwd_dropout(q, k, v, 0.25, 5, 1, scale=0.125)
+    assert torch.equal(a, b) and not torch.equal(a, c)
+    assert pkg.sync_status() == 0
+
+
+def test_bad_probability_is_rejected():
+    pkg = _pkg()
+    x = make_inputs(AttnShape(1, 1, 16, 64), "bf16", seed=9)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    for p in (1.0, -0.5, float("nan"), 0.999):
+        with pytest.raises(pkg.AttnError):
+            pkg.attn_fwd_dropout(q, k, v, p, 1, 0)
+    with pytest.raises(TypeError):
+        pkg.attn_fwd_dropout(q.half(), k.half(), v.half(), 0.1, 1, 0)
