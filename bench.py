@@ -294,6 +294,46 @@ def measure_blocksparse(attn, steps, warmup, peaks, density=0.25):
             "frac": fl / (ms * 1e-3) / 1e12 / peak, "status": attn.sync_status()}
 
 
+def measure_dropout(attn, steps, warmup, peaks, p_drop=0.1):
+    """Dropout forward and backward (p = 0.1, Philox draws in both kernels) on
+    the bench shape, non-causal.  Credited FLOPs are those of the plain path
+    (the draws add no tensor-core work): 4 B H N^2 d forward, 2.5x backward."""
+    import torch
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+    B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
+    x = make_inputs(AttnShape(B, H, N, d), "bf16", seed=4)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    g = [torch.empty_like(q) for _ in range(3)]
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    f_fwd, f_bwd = flops_per_step(B, H, N, d, False)
+
+    def fwd():
+        attn.attn_fwd_dropout(q, k, v, p_drop, 1234, 0, o=o, lse=lse)
+
+    def bwd():
+        attn.attn_bwd_dropout(q, k, v, o, do, lse, p_drop, 1234, 0, dq=g[0], dk=g[1], dv=g[2])
+
+    res = {"workload": "dropout p=%g, B=2 H=16 N=8192 d=128 bf16, non-causal" % p_drop}
+    for name, fn, fl in (("fwd", fwd, f_fwd), ("bwd", bwd, f_bwd)):
+        for _ in range(max(warmup, 3)):
+            fwd()
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        tf = fl / (ms * 1e-3) / 1e12
+        res[name] = {"ms": ms, "tflops": tf, "frac": tf / peak}
+    res["status"] = attn.sync_status()
+    return res
+
+
 def cpu_model():
     try:
         for ln in open("/proc/cpuinfo"):
@@ -458,6 +498,7 @@ def run_ours(args):
     decode = measure_decode(attn, K, args.warmup, peaks) if rank == 0 else None
     fp8 = measure_fp8(attn, K, args.warmup, peaks) if rank == 0 else None
     sparse = measure_blocksparse(attn, K, args.warmup, peaks) if rank == 0 else None
+    dropout = measure_dropout(attn, K, args.warmup, peaks) if rank == 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -477,6 +518,7 @@ def run_ours(args):
                            "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
                            "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
                 "roofline": roof, "cpu_baseline": cpu, "decode": decode, "fp8": fp8, "blocksparse": sparse,
+                "dropout": dropout,
                 "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches, "gpu_launches_e2e": launches_e2e,
