@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, abort_flag, status);
       tc_fence_after_sync();
       int is = 0, ip = 0, iv = 0, ik = 0;
-      uint64_t t_idle = global_timer_ns();
+      IdleWatch watch;
       while (ok && ik < nq) {
         bool progress = false;
         if (ik < iv && ik < ip && mbar_probe(bar(C::B_DSFULL), ik & 1)) {
@@ -376,14 +376,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           progress = true;
         }
         if (progress) {
-          t_idle = global_timer_ns();
-        } else if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
-          *abort_flag = 1;
-          ok = false;
-        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
-          *abort_flag = 1;
-          atomicExch(status, kStatusTimeout);
-          ok = false;
+          watch.progress();
+        } else {
+          ok = watch.idle(abort_flag, status, kWaitLimitNs);
         }
       }
       tc_commit(bar(C::B_MMADONE));

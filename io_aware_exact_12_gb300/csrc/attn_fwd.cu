@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         int js[2] = {0, 0};  // next S index per tile
         int jp[2] = {0, 0};  // next PV index per tile
         int k_rel = 0, v_rel = 0;  // next key/value tile whose stage is still held
-        uint64_t t_idle = global_timer_ns();
+        IdleWatch watch;
         while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
           bool progress = false;
   #pragma unroll
@@ -323,16 +323,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             ++v_rel;
           }
           if (progress) {
-            t_idle = global_timer_ns();
+            watch.progress();
           } else {
-            if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
-              *abort_flag = 1;
-              ok = false;
-            } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
-              *abort_flag = 1;
-              atomicExch(status, kStatusTimeout);
-              ok = false;
-            }
+            ok = watch.idle(abort_flag, status, kWaitLimitNs);
           }
         }
       } else {
@@ -345,7 +338,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
         int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
         int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
-        uint64_t t_idle = global_timer_ns();
+        IdleWatch watch;
         while (ok && (k_rel < npos || v_rel < npos)) {
           bool progress = false;
           // Loads are observed strictly in position order: when position p is
@@ -402,16 +395,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             ++v_rel;
           }
           if (progress) {
-            t_idle = global_timer_ns();
+            watch.progress();
           } else {
-            if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
-              *abort_flag = 1;
-              ok = false;
-            } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
-              *abort_flag = 1;
-              atomicExch(status, kStatusTimeout);
-              ok = false;
-            }
+            ok = watch.idle(abort_flag, status, kWaitLimitNs);
           }
         }
       }

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       tc_fence_after_sync();
       int js[2] = {0, 0}, jp[2] = {0, 0};
       int k_rel = 0, v_rel = 0;
-      uint64_t t_idle = global_timer_ns();
+      IdleWatch watch;
       while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
         bool progress = false;
 #pragma unroll
@@ -280,14 +280,9 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           ++v_rel;
         }
         if (progress) {
-          t_idle = global_timer_ns();
-        } else if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
-          *abort_flag = 1;
-          ok = false;
-        } else if (global_timer_ns() - t_idle > kWaitLimitNs) {
-          *abort_flag = 1;
-          atomicExch(status, kStatusTimeout);
-          ok = false;
+          watch.progress();
+        } else {
+          ok = watch.idle(abort_flag, status, kWaitLimitNs);
         }
       }
       tc_commit(bar(C::B_MMADONE));

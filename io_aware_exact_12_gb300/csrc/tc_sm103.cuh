@@ -80,14 +80,20 @@ __device__ __forceinline__ bool mbar_probe(uint32_t bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Returns false (and
 // raises the abort flag and device status) if it does not within the limit,
 // or if another role of the CTA, or another CTA, already failed.
+// The global status word and the global timer are slow to read (an L2 round
+// trip); a waiter that read them on every poll would notice a completed phase
+// up to that latency late.  They are consulted on every 16th poll only (each
+// poll is a try_wait that suspends in hardware until the phase completes or
+// a short time-out), the shared abort flag on every poll.
 __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
                                                 volatile int* abort_flag, int* status,
                                                 uint64_t limit_ns) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (true) {
+  for (uint32_t n = 1;; ++n) {
     if (mbar_test(bar, parity)) return true;
     if (*abort_flag) return false;
+    if ((n & 15u) != 0) continue;
     if (*reinterpret_cast<volatile int*>(status) != 0) {  // another CTA already failed: stop early
       *abort_flag = 1;
       return false;
@@ -99,6 +105,33 @@ __device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
     }
   }
 }
+
+// Idle bookkeeping for an event loop that polls several barriers without
+// blocking (the single-thread MMA issuers).  progress() after any issue;
+// idle() after a pass that issued nothing returns false when the loop must
+// stop: the CTA aborted, another CTA failed, or nothing happened for
+// limit_ns.  The slow checks run once per 64 idle passes, so the poll that
+// decides when the next MMA group goes out stays a few shared-memory probes.
+struct IdleWatch {
+  uint32_t n = 0;
+  uint64_t t0 = 0;
+  __device__ __forceinline__ void progress() { n = 0; }
+  __device__ __forceinline__ bool idle(volatile int* abort_flag, int* status, uint64_t limit_ns) {
+    if ((++n & 63u) != 0) return true;
+    const uint64_t now = global_timer_ns();
+    if (n == 64u) t0 = now;  // first slow check of this idle stretch starts its clock
+    if (*abort_flag || *reinterpret_cast<volatile int*>(status) != 0) {
+      *abort_flag = 1;
+      return false;
+    }
+    if (now - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicExch(status, kStatusTimeout);
+      return false;
+    }
+    return true;
+  }
+};
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status) {
