@@ -87,8 +87,9 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd.cu", "tc_sm103.cuh"),
-                  "attn_bwd_kernel": ("attn_bwd.cu", "tc_sm103.cuh")}
+KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd.cu", "tc_sm103.cuh", "dropout.cuh"),
+                  "attn_bwd_kernel": ("attn_bwd.cu", "tc_sm103.cuh", "dropout.cuh"),
+                  "attn_decode_split_kernel": ("attn_decode.cu", "tc_sm103.cuh")}
 
 
 def sources_sha(kernel):
@@ -121,8 +122,11 @@ def traffic_from_profiles(kernel, config_key):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms while running.
+    mark_start() / mark_end() bracket the timed region; the summary uses the
+    samples taken inside it (or, for a region shorter than the sampling
+    period, the samples nearest to it, and says so)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -130,6 +134,23 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t_start = None
+        self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+        time.sleep(0.05)  # let the sample that covers the end be written
+
+    @staticmethod
+    def _epoch(ts):
+        import datetime
+        try:
+            return datetime.datetime.strptime(ts.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -137,7 +158,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
         time.sleep(0.3)
@@ -154,23 +175,33 @@ class ClockSampler:
     def summary(self):
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for ln in open(self.path).read().splitlines():
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                rows.append((self._epoch(parts[0]), float(parts[1]), float(parts[2]),
+                             [n for n, val in zip(names, parts[5:9]) if val.lower().startswith("active")]))
             except ValueError:
                 continue
-            for n, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        where = "all samples"
+        sel = rows
+        if self.t_start is not None and self.t_end is not None and all(r[0] is not None for r in rows):
+            inside = [r for r in rows if self.t_start <= r[0] <= self.t_end]
+            if inside:
+                sel, where = inside, "inside the timed region"
+            elif rows:
+                mid = 0.5 * (self.t_start + self.t_end)
+                sel = sorted(rows, key=lambda r: abs(r[0] - mid))[:2]
+                where = "nearest to the timed region (%.0f ms, shorter than the 20 ms period)" % (
+                    1e3 * (self.t_end - self.t_start))
+        sm = [r[1] for r in sel]
+        reasons = sorted({n for r in sel for n in r[3]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": sel[-1][2] if sel else None,
+                "samples": len(sm), "which": where, "reasons": reasons}
 
 
 def oracle_sample(N, d, causal, seed, heads=1):
@@ -222,7 +253,12 @@ def measure_decode(attn, steps, warmup, peaks):
     gbs = nbytes / (ms * 1e-3) / 1e9
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     del k, v
+    # ncu traffic was taken at L = 8192 (1.07 GB, the capture size limit); K/V traffic
+    # grows in proportion to L, so it is scaled to this call's L.
+    t8k = traffic_from_profiles("attn_decode_split_kernel", "b16h16l8192")
+    traffic = None if t8k is None else t8k * L / 8192.0
     return dict(DECODE, ms=ms, bytes_per_call=nbytes, gbs=gbs, bound="hbm", peak_gbs=peak, frac=gbs / peak,
+                traffic=traffic, traffic_note="ncu DRAM bytes at L=8192 scaled by L/8192",
                 status=attn.sync_status())
 
 
@@ -329,7 +365,9 @@ def measure_dropout(attn, steps, warmup, peaks, p_drop=0.1):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
         tf = fl / (ms * 1e-3) / 1e12
-        res[name] = {"ms": ms, "tflops": tf, "frac": tf / peak}
+        kern = "attn_fwd_kernel" if name == "fwd" else "attn_bwd_kernel"
+        res[name] = {"ms": ms, "tflops": tf, "frac": tf / peak,
+                     "traffic": traffic_from_profiles(kern, "c4_noncausal_dropout")}
     res["status"] = attn.sync_status()
     return res
 
@@ -410,6 +448,7 @@ def run_ours(args):
     with ClockSampler(local) as clocks:
         barrier(world)
         torch.cuda.synchronize()
+        clocks.mark_start()
         for i in range(K):
             ev[i][0].record(stream)
             attn.attn_fwd(q, k, v, scale=scale, causal=causal, o=o, lse=lse)
@@ -417,6 +456,7 @@ def run_ours(args):
             attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=causal, dq=dq, dk=dk, dv=dv)
             ev[i][2].record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         barrier(world)
     status = attn.sync_status()
     clk = clocks.summary()
@@ -502,9 +542,9 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, fl, threads = oracle_sample(N, d, causal, seed=4, heads=1)
+        dt, fl, threads = oracle_sample(N, d, causal, seed=4, heads=5)
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "1 of 32 heads (B=1, H=1, N=8192, d=128, non-causal), forward + backward, "
+               "sample": "5 of 32 heads (B=1, H=5, N=8192, d=128, non-causal), forward + backward, "
                          "%.1f s" % dt, "cpu": cpu_model()}
 
     if rank == 0:

@@ -6,6 +6,8 @@ capture can skip them with ``-s``.
   python -m io_aware_exact_12_gb300.profile_case --op bwd ...   (one attn_bwd = 3 launches)
   python -m io_aware_exact_12_gb300.profile_case --op naive ... (materialising 3-step
       torch comparator: S = QK^T, P = softmax(S), O = PV, to measure its DRAM bytes)
+  --op fwd_dropout / bwd_dropout: the dropout entries with p = 0.1
+  --op decode: one query token per head against an N-token cache (B, H, N, d)
 """
 from __future__ import annotations
 
@@ -17,7 +19,8 @@ import torch
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["fwd", "bwd", "naive"], default="fwd")
+    ap.add_argument("--op", choices=["fwd", "bwd", "naive", "fwd_dropout", "bwd_dropout", "decode"],
+                    default="fwd")
     ap.add_argument("--B", type=int, default=2)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=8192)
@@ -34,9 +37,18 @@ def main(argv=None):
     q, k, v, do = x["q"], x["k"], x["v"], x["do"]
     scale = 1.0 / math.sqrt(a.d)
     o, lse = attn.attn_fwd(q, k, v, scale=scale, causal=a.causal)
+    if a.op.endswith("dropout"):
+        o, lse = attn.attn_fwd_dropout(q, k, v, 0.1, 1234, 0, scale=scale, causal=a.causal)
+    q1 = q[:, :, 0].contiguous()
 
     def run():
-        if a.op == "fwd":
+        if a.op == "fwd_dropout":
+            attn.attn_fwd_dropout(q, k, v, 0.1, 1234, 0, scale=scale, causal=a.causal, o=o, lse=lse)
+        elif a.op == "bwd_dropout":
+            attn.attn_bwd_dropout(q, k, v, o, do, lse, 0.1, 1234, 0, scale=scale, causal=a.causal)
+        elif a.op == "decode":
+            attn.attn_decode(q1, k, v, scale=scale)
+        elif a.op == "fwd":
             attn.attn_fwd(q, k, v, scale=scale, causal=a.causal, o=o, lse=lse)
         elif a.op == "bwd":
             attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=a.causal)
