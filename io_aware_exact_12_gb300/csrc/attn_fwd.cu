@@ -73,7 +73,8 @@ struct FwdCfg {
   static constexpr int B_PFULL = B_SFULL + 2;
   static constexpr int B_ODONE = B_PFULL + 2;
   static constexpr int B_MMADONE = B_ODONE + 2;
-  static constexpr int NBAR = B_MMADONE + 1;
+  static constexpr int B_PHALF = B_MMADONE + 1;  // dropout: first 64 keys of P_q written
+  static constexpr int NBAR = B_PHALF + 2;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int OFF_NPOS = OFF_ABORT + 4;                   // int[3]: positions, per-tile counts
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar(C::B_SFULL + q), 1);
       mbar_init(bar(C::B_PFULL + q), C::BM);
+      mbar_init(bar(C::B_PHALF + q), C::BM);
       mbar_init(bar(C::B_ODONE + q), 1);
     }
     mbar_init(bar(C::B_MMADONE), 1);
@@ -274,26 +276,49 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         tc_fence_after_sync();
         int js[2] = {0, 0};  // next S index per tile
         int jp[2] = {0, 0};  // next PV index per tile
+        bool half[2] = {false, false};  // first half of PV_q(jp) issued
         int k_rel = 0, v_rel = 0;  // next key/value tile whose stage is still held
         IdleWatch watch;
         while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
           bool progress = false;
   #pragma unroll
           for (int q = 0; q < 2; ++q) {
-            // PV_q(jp)
+            // PV_q(jp).  With dropout it goes in two halves: keys 0-63 as soon
+            // as the softmax has written that half of P (it draws and writes the
+            // second half meanwhile), keys 64-127 once all of P_q is written.
+            // Without dropout the second half is too short to hide the extra
+            // hand-off, and PV waits for all of P.
             const int jv = jp[q];
-            if (jv < nkv[q] && jv < js[q] &&
+            if (jv < nkv[q] && jv < js[q] && !half[q] &&
                 mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
-                mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
+                mbar_probe(bar((DROP ? C::B_PHALF : C::B_PFULL) + q), jv & 1)) {
+              tc_fence_after_sync();
+              const uint32_t d_o = tmem + 2 * C::BN + q * D;
+              const uint32_t a_p = tmem + q * C::BN;
+              const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+              constexpr int KK_FIRST = DROP ? C::BN / 32 : C::BN / 16;
+  #pragma unroll
+              for (int kk = 0; kk < KK_FIRST; ++kk)
+                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+              if constexpr (DROP) {
+                half[q] = true;
+              } else {
+                tc_commit(bar(C::B_ODONE + q));
+                jp[q] = jv + 1;
+              }
+              progress = true;
+            }
+            if (DROP && half[q] && mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
               tc_fence_after_sync();
               const uint32_t d_o = tmem + 2 * C::BN + q * D;
               const uint32_t a_p = tmem + q * C::BN;
               const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
   #pragma unroll
-              for (int kk = 0; kk < C::BN / 16; ++kk)
-                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = C::BN / 32; kk < C::BN / 16; ++kk)
+                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, 1u);
               tc_commit(bar(C::B_ODONE + q));
               jp[q] = jv + 1;
+              half[q] = false;
               progress = true;
             }
             // S_q(js)
@@ -532,6 +557,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         tmem_st32(tS + c0 * 32, pk);
+        if (DROP && c0 == 0) {  // keys 0-63 of P (and any O correction) are in TMEM
+          tmem_st_wait();
+          tc_fence_before_sync();
+          mbar_arrive(bar(C::B_PHALF + q));
+        }
       }
       l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
       l_round = l_round * alpha + ((sr0 + sr1) + (sr2 + sr3));
