@@ -300,9 +300,10 @@ def measure_fp8(attn, steps, warmup, peaks):
 
 
 def measure_blocksparse(attn, steps, warmup, peaks, density=0.25):
-    """Block-sparse forward on the bench shape with a seeded random block mask
-    of the given density (diagonal always on).  Credited FLOPs count only the
-    enabled 128 x 128 tile pairs (4 * 128 * 128 * d each)."""
+    """Block-sparse forward and backward on the bench shape with a seeded
+    random block mask of the given density (diagonal always on).  Credited
+    FLOPs count only the enabled 128 x 128 tile pairs (4 * 128 * 128 * d each
+    forward, 2.5x that backward)."""
     import torch
     from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
     B, H, N, d = WORKLOAD["B"], WORKLOAD["H"], WORKLOAD["N"], WORKLOAD["d"]
@@ -310,27 +311,41 @@ def measure_blocksparse(attn, steps, warmup, peaks, density=0.25):
     g = torch.Generator().manual_seed(3)
     mask = (torch.rand((H, nb, nb), generator=g) < density).to(torch.uint8)
     mask[:, torch.arange(nb), torch.arange(nb)] = 1
-    x = make_inputs(AttnShape(B, H, N, d), "bf16", seed=4, with_grad=False)
-    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    x = make_inputs(AttnShape(B, H, N, d), "bf16", seed=4)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     m = mask.cuda()
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
-    for _ in range(max(warmup, 3)):
+    g = [torch.empty_like(q) for _ in range(3)]
+
+    def fwd():
         attn.attn_fwd_blocksparse(q, k, v, m, o=o, lse=lse)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        attn.attn_fwd_blocksparse(q, k, v, m, o=o, lse=lse)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+
+    def bwd():
+        attn.attn_bwd_blocksparse(q, k, v, o, do, lse, m, dq=g[0], dk=g[1], dv=g[2])
+
     pairs = int(mask.sum()) * B
     fl = 4.0 * 128 * 128 * d * pairs
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    return {"workload": "block-sparse forward, B=2 H=16 N=8192 d=128 bf16, per-head random mask",
-            "density": pairs / (B * H * nb * nb), "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12,
-            "frac": fl / (ms * 1e-3) / 1e12 / peak, "status": attn.sync_status()}
+    res = {"workload": "block-sparse forward and backward, B=2 H=16 N=8192 d=128 bf16, per-head random mask",
+           "density": pairs / (B * H * nb * nb)}
+    for name, fn, f in (("fwd", fwd, fl), ("bwd", bwd, 2.5 * fl)):
+        for _ in range(max(warmup, 3)):
+            fwd()
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        res[name] = {"ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "frac": f / (ms * 1e-3) / 1e12 / peak}
+    # the forward's figures also at the top level, as before
+    res.update(ms=res["fwd"]["ms"], tflops=res["fwd"]["tflops"], frac=res["fwd"]["frac"])
+    res["status"] = attn.sync_status()
+    return res
 
 
 def measure_dropout(attn, steps, warmup, peaks, p_drop=0.1):

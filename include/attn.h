@@ -140,6 +140,19 @@ int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, f
                          float scale, int causal, void* stream);
 
 /*
+ * Block-sparse backward (bf16): the gradients of attn_fwd_blocksparse's output
+ * for the same block_mask, mask_heads and causal flag (o and lse from that
+ * call).  The CTA of each 128-key tile visits only the query tiles whose mask
+ * entry enables it; a key tile no query tile sees gets dK = dV = 0, and dQ
+ * rows of a query block that sees no key are 0.  Scratch and errors as for
+ * attn_bwd; the mask constraints as for attn_fwd_blocksparse.
+ */
+int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                         float scale, int causal, void* stream);
+
+/*
  * Forward with FP8 (e4m3) inputs: q, k, v are [B, H, N, 128] e4m3 bytes whose
  * real values are descale_q*q, descale_k*k, descale_v*v (per-tensor factors,
  * finite and > 0); o is bf16 [B, H, N, 128], lse fp32 [B, H, N] in the units

@@ -19,7 +19,7 @@ import os
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_dropout.restype = I
         L.attn_fwd_blocksparse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, P]
         L.attn_fwd_blocksparse.restype = I
+        L.attn_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P]
+        L.attn_bwd_blocksparse.restype = I
         L.attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, F, I, P]
         L.attn_fwd_fp8.restype = I
         L.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
@@ -235,6 +237,14 @@ def attn_decode(q, k, v, scale=None, o=None, lse=None, stream=None):
     return o, lse
 
 
+def _check_block_mask(block_mask, H, N):
+    nb = (N + 127) // 128
+    if (not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda or block_mask.dtype != torch.uint8
+            or not block_mask.is_contiguous() or block_mask.dim() != 3
+            or tuple(block_mask.shape[1:]) != (nb, nb) or block_mask.shape[0] not in (1, H)):
+        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [H or 1, %d, %d]" % (nb, nb))
+
+
 def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, lse=None, stream=None):
     """Forward restricted by a block mask: block_mask is a uint8 CUDA tensor
     [H or 1, ceil(N/128), ceil(N/128)]; key j is visible to query i iff
@@ -244,11 +254,7 @@ def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, 
     _check("q", q, None, torch.bfloat16)
     _check("k", k, q, torch.bfloat16)
     _check("v", v, q, torch.bfloat16)
-    nb = (N + 127) // 128
-    if (not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda or block_mask.dtype != torch.uint8
-            or not block_mask.is_contiguous() or block_mask.dim() != 3
-            or tuple(block_mask.shape[1:]) != (nb, nb) or block_mask.shape[0] not in (1, H)):
-        raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [H or 1, %d, %d]" % (nb, nb))
+    _check_block_mask(block_mask, H, N)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q) if o is None else o
@@ -262,6 +268,33 @@ def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, 
     if rc:
         raise AttnError("attn_fwd_blocksparse", rc)
     return o, lse
+
+
+def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=False, dq=None, dk=None, dv=None,
+                         stream=None):
+    """Gradients of attn_fwd_blocksparse's output for the same block_mask and
+    causal flag.  Returns (dq, dk, dv)."""
+    B, H, N, d = _dims(q)
+    _check("q", q, None, torch.bfloat16)
+    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(name, t, q, q.dtype)
+    _check("lse", lse, None, torch.float32)
+    _check_block_mask(block_mask, H, N)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(name, t, q, q.dtype)
+    with torch.cuda.device(q.device):
+        rc = lib().attn_bwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                        block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
+                                        int(bool(causal)), _stream_handle(stream))
+    if rc:
+        raise AttnError("attn_bwd_blocksparse", rc)
+    return dq, dk, dv
 
 
 def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, scale=None, causal=False, o=None, lse=None,

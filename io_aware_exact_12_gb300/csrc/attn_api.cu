@@ -217,7 +217,8 @@ int fwd_entry(const void* q, const void* k, const void* v, void* o, float* lse, 
 
 int bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dO,
               const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-              float scale, int causal, void* stream, bool bf16, const DropParams& drop = kNoDrop) {
+              float scale, int causal, void* stream, bool bf16, const DropParams& drop = kNoDrop,
+              const uint8_t* bmask = nullptr, int mask_heads = 1) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return kStatusInvalid;
   int rc = validate_common(B, H, N, d, scale);
   if (rc) return rc;
@@ -259,6 +260,9 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   a.ws_lse2 = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.lse2_off);
   a.ws_d = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.d_off);
   a.drop = drop;
+  a.bmask = bmask;
+  a.H = H;
+  a.mask_heads = mask_heads;
   rc = launch_bwd(a);
   const cudaError_t fe = cudaFreeAsync(ws, s);
   if (rc == kStatusOk && fe != cudaSuccess) rc = kStatusCuda;
@@ -409,6 +413,17 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
                  int causal, void* stream) {
   return attn::fp8_entry(q, k, v, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale, causal,
                          stream);
+}
+
+int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                         float scale, int causal, void* stream) {
+  if (!block_mask) return attn::kStatusInvalid;
+  if (mask_heads != 1 && mask_heads != H) return attn::kStatusInvalid;
+  if (N > 0 && (N + 127) / 128 > attn::kMaxSparseTiles) return attn::kStatusUnsupported;
+  return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, true,
+                         attn::kNoDrop, block_mask, mask_heads);
 }
 
 int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,

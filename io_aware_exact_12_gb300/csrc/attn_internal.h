@@ -67,6 +67,10 @@ struct BwdArgs {
   float* ws_lse2;
   float* ws_d;
   DropParams drop = {0u, 0u, 0u, 0u, 1.f};
+  // block-sparse only (nullptr otherwise): [mask_heads][nb][nb] bytes, nb = ceil(N/128)
+  const uint8_t* bmask = nullptr;
+  int H = 1;
+  int mask_heads = 1;
 };
 
 // Bytes of backward scratch for a problem, and its carve-up.

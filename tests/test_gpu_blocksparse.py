@@ -114,3 +114,77 @@ def test_sparse_long_sequence_sampled_rows(pkg):
         go = o[0, h, i].double().cpu().numpy()
         assert (np.abs(go - ro[0]) - _half_ulp_bf16(ro[0])).max() <= 1e-2
         assert abs(lse[0, h, i].item() - rl[0]) <= 1e-3
+
+
+# ------------------------------------------------------------------ backward
+# Gradients against the oracle's masked backward (rel Frobenius <= 2e-2, the
+# denominator floored at 1e-3 |dO| where an exact gradient vanishes); key
+# tiles no query tile sees must have dK = dV = 0 exactly, and query blocks that
+# see no key dQ = 0 exactly.
+def _check_bwd(pkg, shape, mask, causal, seed, scale=None):
+    x = make_inputs(shape, "bf16", seed=seed)
+    scale = 1.0 / math.sqrt(shape.d) if scale is None else scale
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    m = mask.cuda()
+    o, lse = pkg.attn_fwd_blocksparse(q, k, v, m, scale=scale, causal=causal)
+    dq, dk, dv = pkg.attn_bwd_blocksparse(q, k, v, o, do, lse, m, scale=scale, causal=causal)
+    assert pkg.sync_status() == 0
+    f = lambda t: t.double().cpu().numpy()  # noqa: E731
+    oo, _ = oracle.forward(f(x["q"]), f(x["k"]), f(x["v"]), scale, causal, block_mask=mask.numpy(), blk=128)
+    ref = oracle.backward(f(x["q"]), f(x["k"]), f(x["v"]), oo, f(x["do"]), scale, causal,
+                          block_mask=mask.numpy(), blk=128)
+    floor = 1e-3 * float(np.linalg.norm(f(x["do"])))
+    for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        e = float(np.linalg.norm(f(g) - r) / max(np.linalg.norm(r), floor))
+        assert e <= 2e-2, "%s rel Frobenius error %g" % (name, e)
+    # exact zeros where the mask leaves nothing
+    N, nb = shape.N, (shape.N + 127) // 128
+    mk = mask.numpy().astype(bool)
+    tri = np.tril(np.ones((nb, nb), dtype=bool)) if causal else np.ones((nb, nb), dtype=bool)
+    for h in range(shape.H):
+        mh = mk[h % mk.shape[0]] & tri
+        for j in np.nonzero(~mh.any(axis=0))[0]:      # key tile seen by no query tile
+            assert not dk[:, h, j * 128:min(N, j * 128 + 128)].any()
+            assert not dv[:, h, j * 128:min(N, j * 128 + 128)].any()
+        for i in np.nonzero(~mh.any(axis=1))[0]:      # query block that sees no key
+            assert not dq[:, h, i * 128:min(N, i * 128 + 128)].any()
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(1000, 128), (640, 64), (300, 32)])
+def test_backward_random_block_masks(pkg, N, d, causal):
+    nb = (N + 127) // 128
+    _check_bwd(pkg, AttnShape(2, 3, N, d), _random_mask(3, nb, 0.4, seed=N + d + 1), causal, seed=N + 1)
+
+
+def test_backward_shared_mask_with_empty_query_block_and_unseen_key_tile(pkg):
+    N, nb = 700, 6
+    mask = _random_mask(1, nb, 0.5, seed=4, keep_diag=False)
+    mask[0, 2, :] = 0  # query block 2 sees nothing
+    mask[0, :, 4] = 0  # key tile 4 is seen by no query block
+    mask[0, 0, 0] = 1
+    for causal in (False, True):
+        _check_bwd(pkg, AttnShape(1, 4, N, 128), mask, causal, seed=6)
+
+
+def test_backward_all_ones_mask_equals_dense(pkg):
+    """Same query tiles in the same order as the dense backward: dK and dV
+    bit-identical; dQ (reduced with atomics in any order) to rounding."""
+    shape = AttnShape(1, 2, 900, 128)
+    x = make_inputs(shape, "bf16", seed=8)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    mask = torch.ones((1, 8, 8), dtype=torch.uint8, device="cuda")
+    for causal in (False, True):
+        o, lse = pkg.attn_fwd(q, k, v, scale=0.1, causal=causal)
+        g1 = pkg.attn_bwd(q, k, v, o, do, lse, scale=0.1, causal=causal)
+        g2 = pkg.attn_bwd_blocksparse(q, k, v, o, do, lse, mask, scale=0.1, causal=causal)
+        assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+        assert (g1[0].float() - g2[0].float()).abs().max().item() <= 1e-2 * g1[0].float().abs().max().item()
+
+
+def test_backward_sparse_longer_sequence(pkg):
+    """N = 4096, 25 %-dense per-head masks, causal and not, against the full oracle."""
+    N, nb = 4096, 32
+    for causal in (False, True):
+        _check_bwd(pkg, AttnShape(1, 2, N, 128), _random_mask(2, nb, 0.25, seed=21 + causal), causal, seed=22)
