@@ -342,6 +342,7 @@ def measure_blocksparse(attn, steps, warmup, peaks, density=0.25):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / steps
         res[name] = {"ms": ms, "tflops": f / (ms * 1e-3) / 1e12, "frac": f / (ms * 1e-3) / 1e12 / peak}
+    res["bwd"]["traffic"] = traffic_from_profiles("attn_bwd_kernel", "c4_noncausal_blocksparse25")
     # the forward's figures also at the top level, as before
     res.update(ms=res["fwd"]["ms"], tflops=res["fwd"]["tflops"], frac=res["fwd"]["frac"])
     res["status"] = attn.sync_status()

@@ -8,6 +8,8 @@ capture can skip them with ``-s``.
       torch comparator: S = QK^T, P = softmax(S), O = PV, to measure its DRAM bytes)
   --op fwd_dropout / bwd_dropout: the dropout entries with p = 0.1
   --op decode: one query token per head against an N-token cache (B, H, N, d)
+  --op fwd_blocksparse / bwd_blocksparse: a seeded random 25 %-dense per-head
+      block mask (diagonal on), as in bench.py
 """
 from __future__ import annotations
 
@@ -19,8 +21,8 @@ import torch
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("--op", choices=["fwd", "bwd", "naive", "fwd_dropout", "bwd_dropout", "decode"],
-                    default="fwd")
+    ap.add_argument("--op", choices=["fwd", "bwd", "naive", "fwd_dropout", "bwd_dropout", "decode",
+                                     "fwd_blocksparse", "bwd_blocksparse"], default="fwd")
     ap.add_argument("--B", type=int, default=2)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=8192)
@@ -40,9 +42,20 @@ def main(argv=None):
     if a.op.endswith("dropout"):
         o, lse = attn.attn_fwd_dropout(q, k, v, 0.1, 1234, 0, scale=scale, causal=a.causal)
     q1 = q[:, :, 0].contiguous()
+    if a.op.endswith("blocksparse"):
+        nb = (a.N + 127) // 128
+        g = torch.Generator().manual_seed(3)
+        mask = (torch.rand((a.H, nb, nb), generator=g) < 0.25).to(torch.uint8)
+        mask[:, torch.arange(nb), torch.arange(nb)] = 1
+        mask = mask.cuda()
+        o, lse = attn.attn_fwd_blocksparse(q, k, v, mask, scale=scale, causal=a.causal)
 
     def run():
-        if a.op == "fwd_dropout":
+        if a.op == "fwd_blocksparse":
+            attn.attn_fwd_blocksparse(q, k, v, mask, scale=scale, causal=a.causal, o=o, lse=lse)
+        elif a.op == "bwd_blocksparse":
+            attn.attn_bwd_blocksparse(q, k, v, o, do, lse, mask, scale=scale, causal=a.causal)
+        elif a.op == "fwd_dropout":
             attn.attn_fwd_dropout(q, k, v, 0.1, 1234, 0, scale=scale, causal=a.causal, o=o, lse=lse)
         elif a.op == "bwd_dropout":
             attn.attn_bwd_dropout(q, k, v, o, do, lse, 0.1, 1234, 0, scale=scale, causal=a.causal)
