@@ -436,11 +436,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const float2 sl2x2 = make_float2(sl2, sl2);
     bool ok = true;
     int qi = i0 - 1;
+    // Dropout: kw[w] holds this key's keep bytes for queries q0 + 4w .. q0 + 4w + 3
+    // of the visit being processed.  The next visit's are drawn ahead, right
+    // after this visit's dS^T is handed over, while the thread would otherwise
+    // wait for the next S^T: each half warp draws 16 query rows for its 16 keys
+    // and transposes the bytes (shuffles; every wait in the loop is made
+    // warp-uniform so that no lane leaves the loop while others shuffle).
+    uint32_t kw[DROP ? 16 : 1];
+    auto draw_visit = [&](int qa) {  // qa: first query of this thread's half
+      if constexpr (DROP) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 r4 = philox4x32_10(
+              make_uint4(static_cast<uint32_t>(kv_row >> 4), static_cast<uint32_t>(qa + 16 * u + (lane & 15)),
+                         static_cast<uint32_t>(bh), drop.offset),
+              drop.k0, drop.k1);
+          uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
+          transpose16x16_bytes(w, lane);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) kw[4 * u + e] = w[e];
+        }
+      }
+    };
+    if (DROP && nq > 0) draw_visit(i0 * C::BM + g * 64);  // dropout is dense: visit it is tile i0 + it
     for (int it = 0; it < nq; ++it) {
       const int s = it % C::NSTQ;
       const int q0 = ATTN_BWD_QTILE(it, qi) * C::BM + g * 64;  // first query of this thread's half
       ok = mbar_wait(bar(C::B_SFULL), it & 1, abort_flag, status);
-      if constexpr (DROP) ok = __all_sync(0xffffffffu, ok);  // the draws below shuffle across the warp
+      if constexpr (DROP) ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
       float p[64];
@@ -466,21 +489,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int c = 0; c < 64; ++c)
           if (c < first) p[c] = 0.f;
       }
-      // keep bytes of this key for queries q0 + 4w .. q0 + 4w + 3 in kw[w]
-      uint32_t kw[16];
-      if constexpr (DROP) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 r4 = philox4x32_10(
-              make_uint4(static_cast<uint32_t>(kv_row >> 4), static_cast<uint32_t>(q0 + 16 * u + (lane & 15)),
-                         static_cast<uint32_t>(bh), drop.offset),
-              drop.k0, drop.k1);
-          uint32_t w[4] = {r4.x, r4.y, r4.z, r4.w};
-          transpose16x16_bytes(w, lane);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) kw[4 * u + e] = w[e];
-        }
-      }
       const uint32_t t2 = drop.t * 0x00010001u;
       {
         uint32_t pk[32];
@@ -496,8 +504,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL));
 
-      if (!(ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status))) break;
-      if (it > 0 && !(ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status))) break;
+      if constexpr (DROP) {  // warp-uniform: the draws at the end of the visit shuffle
+        ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status);
+        if (ok && it > 0) ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      } else {
+        if (!(ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status))) break;
+        if (it > 0 && !(ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status))) break;
+      }
       tc_fence_after_sync();
       const float2* nd = reinterpret_cast<const float2*>(sDD + s * C::BM + g * 64);  // -D
 #pragma unroll
@@ -533,6 +548,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_DSFULL));
+      if (DROP && it + 1 < nq) draw_visit(q0 + C::BM);
     }
     // dK (warpgroup 0) or dV (warpgroup 1) once the last MMAs have completed
     if (ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status)) {

@@ -448,6 +448,25 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int nk = cnt[q];
     int pos = 0;  // position of this tile's next key tile
     const float2 sl2x2 = make_float2(sl2, sl2);
+    // Dropout: the keep bytes of the next key tile are drawn ahead, right after
+    // this tile's P is handed over, while the thread would otherwise wait for
+    // the next S; kb[4 g + w] = word w of the draw for keys 16 g .. 16 g + 15.
+    uint32_t kb[DROP ? 32 : 1];
+    auto draw_tile = [&](int key0) {
+      if constexpr (DROP) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 r4 = philox4x32_10(make_uint4(static_cast<uint32_t>(key0 >> 4) + g, static_cast<uint32_t>(row),
+                                                    static_cast<uint32_t>(bh), drop.offset),
+                                         drop.k0, drop.k1);
+          kb[4 * g] = r4.x;
+          kb[4 * g + 1] = r4.y;
+          kb[4 * g + 2] = r4.z;
+          kb[4 * g + 3] = r4.w;
+        }
+      }
+    };
+    if (nk > 0) draw_tile(0);  // dropout is dense: tile j starts at key j * 128
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
       tc_fence_after_sync();
@@ -540,19 +559,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           }
         }
         if constexpr (DROP) {
-          // keys kv0 + 64 c0 + 16 g + (0..15): one draw; word w covers keys 4w..4w+3
+          // keys kv0 + 64 c0 + 16 g + (0..15): word w of their draw covers keys 4w..4w+3
           const uint32_t t2 = drop.t * 0x00010001u;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            const uint4 r4 = philox4x32_10(
-                make_uint4(static_cast<uint32_t>(kv0 >> 4) + c0 * 4 + g, static_cast<uint32_t>(row),
-                           static_cast<uint32_t>(bh), drop.offset),
-                drop.k0, drop.k1);
-            const uint32_t rw[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-              pk[8 * g + 2 * w] &= ~drop_mask16(drop_lanes(rw[w], kDropSelLo, t2));
-              pk[8 * g + 2 * w + 1] &= ~drop_mask16(drop_lanes(rw[w], kDropSelHi, t2));
+              const uint32_t rw = kb[4 * (4 * c0 + g) + w];
+              pk[8 * g + 2 * w] &= ~drop_mask16(drop_lanes(rw, kDropSelLo, t2));
+              pk[8 * g + 2 * w + 1] &= ~drop_mask16(drop_lanes(rw, kDropSelHi, t2));
             }
           }
         }
@@ -568,6 +583,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL + q));
+      if (DROP && j + 1 < nk) draw_tile((j + 1) * C::BN);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && nk > 0 && mbar_wait(bar(C::B_ODONE + q), (nk - 1) & 1, abort_flag, status)) {
