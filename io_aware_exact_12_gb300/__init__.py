@@ -83,6 +83,26 @@ def last_launch_count() -> int:
     return lib().attn_last_launch_count()
 
 
+class _Nothing:
+    def __enter__(self):
+        return None
+
+    def __exit__(self, *exc):
+        return False
+
+
+_NOTHING = _Nothing()
+
+
+def _on_device(t):
+    """The C ABI works on the current device: switch to t's device only when
+    it is not already current (entering torch.cuda.device costs several us)."""
+    idx = t.device.index
+    if idx is None or idx == torch.cuda.current_device():
+        return _NOTHING
+    return torch.cuda.device(t.device)
+
+
 def _stream_handle(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -123,7 +143,7 @@ def attn_fwd(q, k, v, scale=None, causal=False, o=None, lse=None, stream=None):
     _check("o", o, q, q.dtype)
     _check("lse", lse, None, torch.float32)
     fn = lib().attn_fwd if q.dtype == torch.bfloat16 else lib().attn_fwd_f16
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
                 float(scale), int(bool(causal)), _stream_handle(stream))
     if rc:
@@ -146,7 +166,7 @@ def attn_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(name, t, q, q.dtype)
     fn = lib().attn_bwd if q.dtype == torch.bfloat16 else lib().attn_bwd_f16
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
                 _stream_handle(stream))
@@ -171,7 +191,7 @@ def attn_fwd_dropout(q, k, v, p_drop, seed, offset=0, scale=None, causal=False, 
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     _check("o", o, q, q.dtype)
     _check("lse", lse, None, torch.float32)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib().attn_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
                                     N, d, float(scale), int(bool(causal)), float(p_drop),
                                     int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
@@ -197,7 +217,7 @@ def attn_bwd_dropout(q, k, v, o, do, lse, p_drop, seed, offset=0, scale=None, ca
     dv = torch.empty_like(q) if dv is None else dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(name, t, q, q.dtype)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib().attn_bwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                                     lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
                                     float(scale), int(bool(causal)), float(p_drop),
@@ -229,7 +249,7 @@ def attn_decode(q, k, v, scale=None, o=None, lse=None, stream=None):
     lse = torch.empty((B, H), dtype=torch.float32, device=q.device) if lse is None else lse
     _check("o", o, q, torch.bfloat16)
     _check("lse", lse, None, torch.float32)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib().attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Lk,
                                d, float(scale), _stream_handle(stream))
     if rc:
@@ -261,7 +281,7 @@ def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, 
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check("o", o, q, torch.bfloat16)
     _check("lse", lse, None, torch.float32)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib().attn_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                         block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
                                         int(bool(causal)), _stream_handle(stream))
@@ -287,7 +307,7 @@ def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=Fal
     dv = torch.empty_like(q) if dv is None else dv
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(name, t, q, q.dtype)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib().attn_bwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
                                         lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                         block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
@@ -314,7 +334,7 @@ def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, scale=None, causal=Fa
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check("o", o, None, torch.bfloat16)
     _check("lse", lse, None, torch.float32)
-    with torch.cuda.device(q.device):
+    with _on_device(q):
         rc = lib().attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), float(descale_q), float(descale_k),
                                 float(descale_v), o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale),
                                 int(bool(causal)), _stream_handle(stream))

@@ -140,8 +140,27 @@ bool ensure_smem_attr(const void* func, int bytes) {
 }
 
 bool check_launch_regs(const void* func, int regs) {
+  // The register count is a property of the compiled kernel: look it up once
+  // per kernel (cudaFuncGetAttributes costs about a microsecond per call).
+  static std::mutex mu;
+  static const void* seen_func[64] = {};
+  static int seen_regs[64] = {};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < 64 && seen_func[i]; ++i)
+      if (seen_func[i] == func) return seen_regs[i] == regs;
+  }
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  for (int i = 0; i < 64; ++i) {
+    if (seen_func[i] == func) break;
+    if (!seen_func[i]) {
+      seen_func[i] = func;
+      seen_regs[i] = fa.numRegs;
+      break;
+    }
+  }
   return fa.numRegs == regs;
 }
 
