@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -92,14 +93,23 @@ KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd.cu", "tc_sm103.cuh", "dropout.cu
                   "attn_decode_split_kernel": ("attn_decode.cu", "tc_sm103.cuh")}
 
 
+def code_only(text):
+    """Source text without comments and with whitespace collapsed, so that an
+    edit of comments alone does not count as a change of the kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def sources_sha(kernel):
-    """Short hash of the device source files a kernel is built from."""
+    """Short hash of the code (comments stripped) of the device source files a
+    kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "io_aware_exact_12_gb300", "csrc")
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, name), "rb") as f:
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

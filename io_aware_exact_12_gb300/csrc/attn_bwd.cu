@@ -43,11 +43,12 @@
 //                         dV [256+D,256+2D).
 // Causal: key tile j only visits query tiles i >= j; the diagonal tile is
 // masked elementwise (P^T[key][query] = 0 when key > query).
-// Dropout (DROP): the keep bytes of the forward are drawn again (dropout.cuh):
-// each half warp draws 16 query rows for its 16 keys and transposes them so a
-// thread holds its key's bytes; dropped P^T entries are cleared before the dV
-// product (dV scaled by 256 / t at the end) and dP^T is weighted by
-// keep * 256 / t in dS^T = P^T o (w dP^T - D).
+// Dropout (DROP): the keep bytes of the forward are drawn again (dropout.cuh),
+// one visit ahead while the warps wait for the next S^T: each half warp draws
+// 16 query rows for its 16 keys and transposes them so a thread holds its
+// key's bytes; dropped P^T entries are cleared before the dV product (dV
+// scaled by 256 / t at the end) and dP^T is weighted by keep * 256 / t in
+// dS^T = P^T o (w dP^T - D).  Block-sparse (SPARSE): see attn_bwd_kernel.
 #include "attn_internal.h"
 #include "dropout.cuh"
 #include "tc_sm103.cuh"

@@ -32,10 +32,12 @@
 //   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied; only the diagonal tile (and the ragged last tile) are masked.
-// Dropout (DROP): after P is rounded and summed into l, each thread draws the
-// keep bytes of its row (one Philox call per 16 keys, dropout.cuh) and clears
-// the dropped halves of the packed P before it goes to TMEM; the epilogue
-// folds 256 / t into 1 / l.  m, l and LSE stay those of the undropped softmax.
+// Dropout (DROP): after P is rounded and summed into l, each thread clears
+// the dropped halves of its packed P before it goes to TMEM, from keep bytes
+// drawn for its row (one Philox call per 16 keys, dropout.cuh) while it was
+// waiting for this tile's S; the P V product starts on keys 0-63 while the
+// second half is masked, and the epilogue folds 256 / t into 1 / l.  m, l and
+// LSE stay those of the undropped softmax.
 #include "attn_internal.h"
 #include "dropout.cuh"
 #include "tc_sm103.cuh"
