@@ -10,6 +10,7 @@ capture can skip them with ``-s``.
   --op decode: one query token per head against an N-token cache (B, H, N, d)
   --op fwd_blocksparse / bwd_blocksparse: a seeded random 25 %-dense per-head
       block mask (diagonal on), as in bench.py
+  --op fwd_fp8: the e4m3 forward (d = 128) on per-tensor-quantised inputs
 """
 from __future__ import annotations
 
@@ -22,7 +23,7 @@ import torch
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", choices=["fwd", "bwd", "naive", "fwd_dropout", "bwd_dropout", "decode",
-                                     "fwd_blocksparse", "bwd_blocksparse"], default="fwd")
+                                     "fwd_blocksparse", "bwd_blocksparse", "fwd_fp8"], default="fwd")
     ap.add_argument("--B", type=int, default=2)
     ap.add_argument("--H", type=int, default=16)
     ap.add_argument("--N", type=int, default=8192)
@@ -42,6 +43,11 @@ def main(argv=None):
     if a.op.endswith("dropout"):
         o, lse = attn.attn_fwd_dropout(q, k, v, 0.1, 1234, 0, scale=scale, causal=a.causal)
     q1 = q[:, :, 0].contiguous()
+    if a.op == "fwd_fp8":
+        from io_aware_exact_12_gb300.synth import make_inputs_fp8
+        x8 = make_inputs_fp8(AttnShape(a.B, a.H, a.N, a.d), seed=4)
+        q8, k8, v8 = (x8[n][0].cuda() for n in ("q", "k", "v"))
+        sq, sk, sv = x8["q"][1], x8["k"][1], x8["v"][1]
     if a.op.endswith("blocksparse"):
         nb = (a.N + 127) // 128
         g = torch.Generator().manual_seed(3)
@@ -51,7 +57,9 @@ def main(argv=None):
         o, lse = attn.attn_fwd_blocksparse(q, k, v, mask, scale=scale, causal=a.causal)
 
     def run():
-        if a.op == "fwd_blocksparse":
+        if a.op == "fwd_fp8":
+            attn.attn_fwd_fp8(q8, k8, v8, sq, sk, sv, causal=a.causal, o=o, lse=lse)
+        elif a.op == "fwd_blocksparse":
             attn.attn_fwd_blocksparse(q, k, v, mask, scale=scale, causal=a.causal, o=o, lse=lse)
         elif a.op == "bwd_blocksparse":
             attn.attn_bwd_blocksparse(q, k, v, o, do, lse, mask, scale=scale, causal=a.causal)
