@@ -19,7 +19,7 @@ import os
 
 import torch
 
-__all__ = ["attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attention", "attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -341,6 +341,44 @@ def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, scale=None, causal=Fa
     if rc:
         raise AttnError("attn_fwd_fp8", rc)
     return o, lse
+
+
+class _Attention(torch.autograd.Function):
+    """Differentiable exact attention: forward through attn_fwd (or
+    attn_fwd_dropout), backward through attn_bwd (or attn_bwd_dropout) from
+    the saved O and LSE (P is recomputed, never stored)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal, p_drop, seed, offset):
+        q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+        if p_drop > 0.0:
+            o, lse = attn_fwd_dropout(q, k, v, p_drop, seed, offset, scale=scale, causal=causal)
+        else:
+            o, lse = attn_fwd(q, k, v, scale=scale, causal=causal)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.args = (scale, causal, p_drop, seed, offset)
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        scale, causal, p_drop, seed, offset = ctx.args
+        do = do.contiguous()
+        if p_drop > 0.0:
+            dq, dk, dv = attn_bwd_dropout(q, k, v, o, do, lse, p_drop, seed, offset, scale=scale, causal=causal)
+        else:
+            dq, dk, dv = attn_bwd(q, k, v, o, do, lse, scale=scale, causal=causal)
+        return dq, dk, dv, None, None, None, None, None
+
+
+def attention(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0):
+    """O = softmax(scale q k^T [+ causal mask]) v as a differentiable op on
+    [B, H, N, d] CUDA tensors (bf16/fp16; with dropout, bf16).  Gradients
+    flow to q, k and v through the recomputation backward.  With dropout_p > 0
+    the keep decisions come from (seed, offset); use a new offset per step."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    return _Attention.apply(q, k, v, float(scale), bool(causal), float(dropout_p), int(seed), int(offset))
 
 
 def sync_status(stream=None) -> int:
