@@ -230,13 +230,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     const float* __restrict__ dvec, float* __restrict__ dq_acc,
                     uint8_t* __restrict__ dk_out, uint8_t* __restrict__ dv_out, int N, int Npad,
                     float sl2, float scale, int causal, int negate, int* status,
-                    DropParams drop, const uint8_t* __restrict__ bmask, int H, int mask_heads) {
+                    DropParams drop, const uint8_t* __restrict__ bmask, int H, int mask_heads,
+                    int head_group) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int jt = blockIdx.x;  // key tile (heaviest first under the causal mask)
-  const int bh = blockIdx.y;
+  int jt = blockIdx.x, bh = blockIdx.y;  // key tile, head
+  if (causal)  // key tile 0 sees every query tile: heaviest (of a group of heads) first
+    grouped_rank_order(blockIdx.x + blockIdx.y * gridDim.x, gridDim.x, gridDim.y, head_group, jt, bh);
   const int kv0 = jt * C::BN;
   const int ntq = (N + C::BM - 1) / C::BM;
   const int i0 = causal ? jt : 0;
@@ -655,7 +657,7 @@ int launch_bwd_t(const BwdArgs& a) {
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, mdo, a.ws_lse2, a.ws_d, a.ws_dq, static_cast<uint8_t*>(a.dk),
       static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status, a.drop,
-      a.bmask, a.H, a.mask_heads);
+      a.bmask, a.H, a.mask_heads, order_head_group(a.BH, int64_t{8} * a.N * D, int64_t{32} << 20));
   {
     const int64_t groups = static_cast<int64_t>(a.BH) * a.N * D / 8;
     const int blocks = static_cast<int>(std::min<int64_t>((groups + 255) / 256, 152 * 16));

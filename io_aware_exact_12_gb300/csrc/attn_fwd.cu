@@ -132,13 +132,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_v, uint8_t* __restrict__ o_out,
                     float* __restrict__ lse_out, int N, float sl2, int causal, int negate,
                     const uint8_t* __restrict__ bmask, int H, int mask_heads, int* status,
-                    DropParams drop) {
+                    DropParams drop, int head_group) {
   using C = FwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int qb = causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;  // heavy tiles first
+  int bh = blockIdx.y, qb = blockIdx.x;
+  if (causal) {  // heaviest query blocks (of a group of heads) first
+    int rank;
+    grouped_rank_order(blockIdx.x + blockIdx.y * gridDim.x, gridDim.x, gridDim.y, head_group, rank, bh);
+    qb = gridDim.x - 1 - rank;
+  }
   const int nkv_all = (N + C::BN - 1) / C::BN;
   int nkv[2];
 #pragma unroll
@@ -640,7 +644,8 @@ int launch_fwd_t(const FwdArgs& a) {
   dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, static_cast<uint8_t*>(a.o), a.lse,
                                                       a.N, a.sl2, a.causal, a.negate, a.bmask, a.H,
-                                                      a.mask_heads, a.status, a.drop);
+                                                      a.mask_heads, a.status, a.drop,
+                                                      order_head_group(a.BH, int64_t{4} * a.N * D, int64_t{128} << 20));
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }
 

@@ -138,14 +138,18 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_vt, uint8_t* __restrict__ o_out,
                         float* __restrict__ lse_out, int N, float sl2, float descale_v, int causal,
-                        int* status) {
+                        int* status, int head_group) {
   using C = Fp8Cfg;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int qb = causal ? (gridDim.x - 1 - blockIdx.x) : blockIdx.x;
+  int bh = blockIdx.y, qb = blockIdx.x;
+  if (causal) {  // heaviest query blocks (of a group of heads) first
+    int rank;
+    grouped_rank_order(blockIdx.x + blockIdx.y * gridDim.x, gridDim.x, gridDim.y, head_group, rank, bh);
+    qb = gridDim.x - 1 - rank;
+  }
   const int nkv_all = (N + C::BN - 1) / C::BN;
   int nkv[2];
 #pragma unroll
@@ -451,7 +455,8 @@ int launch_fwd_fp8(const Fp8Args& a) {
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
   kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mvt, static_cast<uint8_t*>(a.o), a.lse, a.N,
-                                                      a.sl2, a.descale_v, a.causal, a.status);
+                                                      a.sl2, a.descale_v, a.causal, a.status,
+                                                      order_head_group(a.BH, int64_t{2} * a.N * C::D, int64_t{128} << 20));
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }
 
