@@ -88,8 +88,8 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd.cu", "tc_sm103.cuh", "dropout.cuh"),
-                  "attn_bwd_kernel": ("attn_bwd.cu", "tc_sm103.cuh", "dropout.cuh"),
+KERNEL_SOURCES = {"attn_fwd_kernel": ("attn_fwd.cu", "block_order.h", "tc_sm103.cuh", "dropout.cuh"),
+                  "attn_bwd_kernel": ("attn_bwd.cu", "block_order.h", "tc_sm103.cuh", "dropout.cuh"),
                   "attn_decode_split_kernel": ("attn_decode.cu", "tc_sm103.cuh")}
 
 

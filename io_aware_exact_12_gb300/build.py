@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libattn.so")
 SOURCES = ["attn_api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_noalloc.cu", "attn_diag.cu", "attn_decode.cu", "attn_fwd_fp8.cu"]
-HEADERS = ["attn_internal.h", "tc_sm103.cuh", "dropout.cuh"]
+HEADERS = ["attn_internal.h", "block_order.h", "tc_sm103.cuh", "dropout.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

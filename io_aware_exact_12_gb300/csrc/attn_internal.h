@@ -8,6 +8,8 @@
 
 #include <algorithm>
 
+#include "block_order.h"
+
 namespace attn {
 
 // Status codes; the public values are those of attn_status_t in attn.h.
@@ -31,32 +33,6 @@ struct DropParams {
   uint32_t offset;     // fourth counter word
   float rscale;
 };
-
-// Block order of the causal kernels.  Under the causal mask a block's work
-// grows with its distance from the diagonal; issued head after head, the
-// heaviest blocks of the last heads would start last and leave SMs idle at the
-// end.  Linear block index L (blockIdx.x fastest) is mapped instead so that
-// within each group of g heads every head's heaviest block comes first, then
-// every head's next-heaviest, and so on: rank 0 is the heaviest block of its
-// head.  g keeps the operands of the heads in flight a small part of L2.
-__host__ __device__ inline void grouped_rank_order(int L, int nblk, int BH, int g, int& rank, int& bh) {
-  const int grp = L / (g * nblk);
-  const int rem = L - grp * g * nblk;
-  const int gl = (BH - grp * g < g) ? BH - grp * g : g;  // heads in this (possibly last, short) group
-  rank = rem / gl;
-  bh = grp * g + (rem - rank * gl);
-}
-
-// Heads per group for grouped_rank_order: as many as keep `bytes_per_head`
-// of streamed operands within `budget` bytes, at least one.  The forward
-// (read-only K/V) measured best with the group as large as L2 (128 MB), the
-// backward (dQ reductions into the same lines) with 32 MB.
-inline int order_head_group(int BH, int64_t bytes_per_head, int64_t budget) {
-  int64_t g = bytes_per_head > 0 ? budget / bytes_per_head : BH;
-  if (g < 1) g = 1;
-  if (g > BH) g = BH;
-  return static_cast<int>(g);
-}
 
 struct FwdArgs {
   const void *q, *k, *v;

@@ -1,12 +1,12 @@
 // Host check of the causal kernels' block order (grouped_rank_order,
-// order_head_group in attn_internal.h): for every grid of nblk x BH blocks
+// order_head_group in block_order.h): for every grid of nblk x BH blocks
 // and every head-group size, the linear block indices map one-to-one onto
 // (rank, head) pairs, ranks run heaviest-first within a group, and a group
 // holds at most g heads.  Prints "ok" and exits 0 when every case holds.
 #include <cstdio>
 #include <vector>
 
-#include "attn_internal.h"
+#include "block_order.h"
 
 int main() {
   int cases = 0;

@@ -4,22 +4,15 @@ same header function for the host (tests/block_order_check.cpp) and checks
 that it is a bijection onto every (rank, head) pair for many grid shapes and
 head-group sizes, with ranks non-decreasing within a group."""
 import os
-import shutil
 import subprocess
-
-import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_grouped_rank_order_is_a_bijection(tmp_path):
-    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
-    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "include")
-    if not os.path.exists(os.path.join(inc, "cuda_runtime.h")):
-        pytest.skip("CUDA runtime headers not found")
     exe = str(tmp_path / "block_order_check")
     cmd = ["g++", "-std=c++17", "-O1", "-Wall", "-I", os.path.join(ROOT, "io_aware_exact_12_gb300", "csrc"),
-           "-I", inc, os.path.join(ROOT, "tests", "block_order_check.cpp"), "-o", exe]
+           os.path.join(ROOT, "tests", "block_order_check.cpp"), "-o", exe]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
