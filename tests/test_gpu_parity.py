@@ -203,6 +203,31 @@ def test_c5_very_long_sequence():
     _check_identities(x, grads)
 
 
+# The causal kernels visit blocks heaviest first within groups of heads.  The
+# backward groups 32 MB / (8 N d bytes) heads: 4 at N = 8192, d = 128, so 10
+# heads make groups of 4, 4 and 2; the forward groups 128 MB / (4 N d bytes):
+# 8 at N = 32768, so 10 heads make 8 and 2.  Outputs are preset to NaN, so a
+# block the order skipped would show; every row and key column is covered by
+# the LSE finiteness and the per-head identities, sampled ones by the oracle.
+@pytest.mark.parametrize("N", [8192, 32768])
+def test_causal_order_short_last_head_group(N):
+    pkg = _pkg()
+    x = make_inputs(AttnShape(1, 10, N, 128), "bf16", seed=6)
+    s = 1.0 / math.sqrt(128)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), device="cuda")
+    pkg.attn_fwd(q, k, v, scale=s, causal=True, o=o, lse=lse)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    pkg.attn_bwd(q, k, v, o, do, lse, scale=s, causal=True, dq=dq, dk=dk, dv=dv)
+    assert pkg.sync_status() == 0
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+    grads = (dq, dk, dv)
+    _check_sampled(x, s, True, o, lse, grads, nrows=256, heads_for_cols=[9], ncols=32)
+    _check_identities(x, grads)
+
+
 # ------------------------------------------------------------- edge cases
 @pytest.mark.parametrize("N", [1, 2, 63, 127, 129, 255, 257, 383])
 @pytest.mark.parametrize("d", [32, 64, 128])
