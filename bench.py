@@ -275,6 +275,37 @@ def measure_decode(attn, steps, warmup, peaks):
                 status=attn.sync_status())
 
 
+def measure_exp_bound(attn, B, H, N, fwd_ms, bwd_ms):
+    """Secondary bound of the softmax step: one exp2 per score, B*H*N^2 in the
+    forward and as many again in the backward (recomputing P).  The rate of
+    the exponential unit is measured with the library's probe kernel (the
+    same ex2.approx.f32 instruction), enough blocks for 8 per SM."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    blocks, iters = sms * 8, 4096
+    sink = torch.empty(blocks * attn.EX2_PROBE_THREADS, device="cuda", dtype=torch.float32)
+    for _ in range(2):
+        n_exp = attn.probe_ex2(sink, blocks, iters)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    e0.record()
+    for _ in range(reps):
+        attn.probe_ex2(sink, blocks, iters)
+    e1.record()
+    torch.cuda.synchronize()
+    rate = n_exp * reps / (e0.elapsed_time(e1) * 1e-3)  # exponentials per second
+    sink_ok = bool(torch.isfinite(sink).all().item())
+    exps = float(B * H * N * N)
+    fwd_rate, bwd_rate = exps / (fwd_ms * 1e-3), exps / (bwd_ms * 1e-3)
+    return {"unit": "exp2/s", "probe_rate": rate,
+            "exps_per_pass": exps,
+            "fwd": {"rate": fwd_rate, "frac": fwd_rate / rate, "floor_ms": exps / rate * 1e3},
+            "bwd": {"rate": bwd_rate, "frac": bwd_rate / rate, "floor_ms": exps / rate * 1e3},
+            "probe": "%d blocks x 256 threads x %d rounds x 8 chains of ex2.approx.f32" % (blocks, iters),
+            "probe_output_finite": sink_ok, "status": attn.sync_status()}
+
+
 def measure_fp8(attn, steps, warmup, peaks):
     """FP8 forward on the bench shape (B=2 H=16 N=8192 d=128), non-causal and
     causal, against the fp8 dense peak = measured bf16 peak x 2 (the nominal
@@ -633,6 +664,7 @@ def run_ours(args):
     fp8 = measure_fp8(attn, K, args.warmup, peaks) if rank == 0 else None
     sparse = measure_blocksparse(attn, K, args.warmup, peaks) if rank == 0 else None
     dropout = measure_dropout(attn, K, args.warmup, peaks) if rank == 0 else None
+    exp_bound = measure_exp_bound(attn, B, H, N, fwd_ms, bwd_ms) if rank == 0 else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -652,7 +684,7 @@ def run_ours(args):
                            "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
                            "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
                 "roofline": roof, "cpu_baseline": cpu, "decode": decode, "fp8": fp8, "blocksparse": sparse,
-                "dropout": dropout,
+                "dropout": dropout, "exp_bound": exp_bound,
                 "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "pipeline": "%d head-chunks: copies in / compute (%d streams) / copies out overlapped" % (

@@ -228,6 +228,21 @@ int attn_sync_status(void* stream);
  */
 int attn_debug_wait_timeout(int limit_us, void* stream);
 
+/*
+ * Throughput probe of the exponential unit (a measurement aid; the pages have
+ * no counterpart).  The softmax step needs one exp2 per score (B*H*N^2 per
+ * forward, as many again in the backward's recomputation of P), so the
+ * unit's rate bounds both passes next to the tensor cores.  Enqueues one
+ * kernel of `blocks` x 256 threads; each thread runs `iters` rounds of 8
+ * independent ex2.approx.f32 (the instruction the attention kernels use) and
+ * writes one float to `sink`: caller-owned device memory of blocks * 256
+ * floats, 4-byte aligned, overwritten.  Exponentials per launch =
+ * blocks * 256 * iters * 8; time the launch with events on `stream`.
+ * blocks 1 .. 65535, iters 1 .. 2^20, else ATTN_ERR_INVALID_ARG (nothing
+ * enqueued).  Returns ATTN_OK once the kernel is enqueued.
+ */
+int attn_probe_ex2(float* sink, int blocks, int iters, void* stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_string(int status);
 

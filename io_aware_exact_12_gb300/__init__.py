@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.attn_status_string.restype = ctypes.c_char_p
         L.attn_last_launch_count.argtypes = []
         L.attn_last_launch_count.restype = I
+        L.attn_probe_ex2.argtypes = [P, I, I, P]
+        L.attn_probe_ex2.restype = I
         _lib = L
     return _lib
 
@@ -81,6 +83,25 @@ def status_string(code: int) -> str:
 
 def last_launch_count() -> int:
     return lib().attn_last_launch_count()
+
+
+EX2_PROBE_THREADS = 256
+EX2_PROBE_CHAINS = 8
+
+
+def probe_ex2(sink, blocks, iters, stream=None):
+    """Enqueue the exponential-unit throughput probe (attn_probe_ex2) writing
+    one float per thread into `sink` (a float32 CUDA tensor of at least
+    blocks * 256 elements).  Returns the number of exponentials it computes."""
+    if not isinstance(sink, torch.Tensor) or not sink.is_cuda or sink.dtype != torch.float32:
+        raise TypeError("sink must be a float32 CUDA tensor")
+    if not sink.is_contiguous() or sink.numel() < blocks * EX2_PROBE_THREADS:
+        raise ValueError("sink must be contiguous with at least blocks * 256 elements")
+    with _on_device(sink):
+        rc = lib().attn_probe_ex2(sink.data_ptr(), int(blocks), int(iters), _stream_handle(stream))
+    if rc != 0:
+        raise RuntimeError("attn_probe_ex2: %s" % status_string(rc))
+    return blocks * EX2_PROBE_THREADS * iters * EX2_PROBE_CHAINS
 
 
 class _Nothing:

@@ -90,6 +90,15 @@ def test_bwd_rejects_bad_arguments(L):
     assert bwd(lse=FAKE + 0x500002) == 1       # lse not 4-byte aligned
 
 
+def test_ex2_probe_rejects_bad_arguments(L):
+    assert L.attn_probe_ex2(None, 1, 1, None) == 1
+    assert L.attn_probe_ex2(FAKE, 0, 1, None) == 1
+    assert L.attn_probe_ex2(FAKE, 65536, 1, None) == 1
+    assert L.attn_probe_ex2(FAKE, 1, 0, None) == 1
+    assert L.attn_probe_ex2(FAKE, 1, (1 << 20) + 1, None) == 1
+    assert L.attn_probe_ex2(FAKE + 2, 1, 1, None) == 1  # not 4-byte aligned
+
+
 def test_valid_arguments_without_gpu_report_an_error(L):
     import torch
     if torch.cuda.is_available():
