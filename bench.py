@@ -233,8 +233,8 @@ def oracle_sample(N, d, causal, seed, heads=1):
     return dt, f + b, threads
 
 
-E2E_CHUNKS = 8  # head-chunks of the pipelined end-to-end step
-E2E_COMPUTE_STREAMS = 4
+E2E_CHUNKS = 16  # head-chunks of the pipelined end-to-end step
+E2E_COMPUTE_STREAMS = 8
 
 DECODE = {"workload": "decode: 1 query token per (b, h) against a bf16 KV cache, B=16 H=16 L=32768 d=128",
           "B": 16, "H": 16, "L": 32768, "d": 128}
