@@ -392,8 +392,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           ++iv;
           progress = true;
         }
-        if (is < nq && is == iv && mbar_probe(bar(C::B_QFULL + is % C::NSTQ), (is / C::NSTQ) & 1) &&
-            (is == 0 || mbar_probe(bar(C::B_DVDONE), (is - 1) & 1))) {
+        // (the barrier that usually decides is probed first: Q_i, dO_i have long landed)
+        if (is < nq && is == iv && (is == 0 || mbar_probe(bar(C::B_DVDONE), (is - 1) & 1)) &&
+            mbar_probe(bar(C::B_QFULL + is % C::NSTQ), (is / C::NSTQ) & 1)) {
           tc_fence_after_sync();
           const uint32_t q_s = sQ + (is % C::NSTQ) * C::TILE_BYTES;
 #pragma unroll
@@ -404,8 +405,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           ++is;
           progress = true;
         }
-        if (ip < nq && ip == ik && mbar_probe(bar(C::B_QFULL + ip % C::NSTQ), (ip / C::NSTQ) & 1) &&
-            (ip == 0 || mbar_probe(bar(C::B_DQEMPTY), (ip - 1) & 1))) {
+        if (ip < nq && ip == ik && (ip == 0 || mbar_probe(bar(C::B_DQEMPTY), (ip - 1) & 1)) &&
+            mbar_probe(bar(C::B_QFULL + ip % C::NSTQ), (ip / C::NSTQ) & 1)) {
           tc_fence_after_sync();
           const uint32_t do_s = sDO + (ip % C::NSTQ) * C::TILE_BYTES;
 #pragma unroll
