@@ -42,7 +42,8 @@
 //   * TMEM (512 columns): S^T/P^T [0,128) dP^T/dQ [128,256) dK [256,256+D)
 //                         dV [256+D,256+2D).
 // Causal: key tile j only visits query tiles i >= j; the diagonal tile is
-// masked elementwise (P^T[key][query] = 0 when key > query).
+// masked elementwise (P^T[key][query] = 0 when key > query), and the CTAs run
+// heaviest first across a group of heads (block_order.h).
 // Dropout (DROP): the keep bytes of the forward are drawn again (dropout.cuh),
 // one visit ahead while the warps wait for the next S^T: each half warp draws
 // 16 query rows for its 16 keys and transposes them so a thread holds its

@@ -31,7 +31,8 @@
 //               values (the weights actually applied to V) to normalise O.
 //   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 // Causal: key tiles entirely above the diagonal are never loaded or
-// multiplied; only the diagonal tile (and the ragged last tile) are masked.
+// multiplied; only the diagonal tile (and the ragged last tile) are masked;
+// the CTAs run heaviest first across a group of heads (block_order.h).
 // Dropout (DROP): after P is rounded and summed into l, each thread clears
 // the dropped halves of its packed P before it goes to TMEM, from keep bytes
 // drawn for its row (one Philox call per 16 keys, dropout.cuh) while it was
