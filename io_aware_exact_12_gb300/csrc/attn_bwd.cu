@@ -344,7 +344,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
     } else if (warp == 13 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
-      // Four chains over the query tiles i, each group issued as soon as ready:
+      // Four chains over the query tiles i, each group issued as soon as ready
+      // (checked in pipeline order: S, dP, dV, then dK/dQ, which measured 0.5-3 %
+      // faster than the reverse order):
       //   S(i)  = K Q_i^T   needs Q_i resident and dV(i-1) complete (P^T aliases S^T)
       //   dP(i) = V dO_i^T  needs dO_i resident and dQ(i-1) read out (dQ aliases dP^T)
       //   dV(i)             needs P^T(i) in TMEM
@@ -360,39 +362,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       IdleWatch watch;
       while (ok && ik < nq) {
         bool progress = false;
-        if (ik < iv && ik < ip && mbar_probe(bar(C::B_DSFULL), ik & 1)) {
-          tc_fence_after_sync();
-          const uint32_t q_s = sQ + (ik % C::NSTQ) * C::TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk)
-            mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
-                   (ik > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < C::BN / 16; ++kk) {
-            if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: both operands MN-major
-              mma_ss(tmem + C::T_DP, desc_mn_tile<D>(sK, kk), desc_ds_mnmajor(sDS, kk), id_dq,
-                     kk > 0 ? 1u : 0u);
-            else                    // dQ = dS K
-              mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
-                     kk > 0 ? 1u : 0u);
-          }
-          tc_commit(bar(C::B_DQFULL));
-          tc_commit(bar(C::B_QEMPTY + ik % C::NSTQ));
-          tc_commit(bar(C::B_DSEMPTY));
-          ++ik;
-          progress = true;
-        }
-        if (iv < is && mbar_probe(bar(C::B_PFULL), iv & 1)) {
-          tc_fence_after_sync();
-          const uint32_t do_s = sDO + (iv % C::NSTQ) * C::TILE_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < C::BM / 16; ++kk)
-            mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                   desc_mn_tile<D>(do_s, kk), id_dv, (iv > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(C::B_DVDONE));
-          ++iv;
-          progress = true;
-        }
         // (the barrier that usually decides is probed first: Q_i, dO_i have long landed)
         if (is < nq && is == iv && (is == 0 || mbar_probe(bar(C::B_DVDONE), (is - 1) & 1)) &&
             mbar_probe(bar(C::B_QFULL + is % C::NSTQ), (is / C::NSTQ) & 1)) {
@@ -416,6 +385,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                    kk > 0 ? 1u : 0u);
           tc_commit(bar(C::B_DPFULL));
           ++ip;
+          progress = true;
+        }
+        if (iv < is && mbar_probe(bar(C::B_PFULL), iv & 1)) {
+          tc_fence_after_sync();
+          const uint32_t do_s = sDO + (iv % C::NSTQ) * C::TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                   desc_mn_tile<D>(do_s, kk), id_dv, (iv > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(bar(C::B_DVDONE));
+          ++iv;
+          progress = true;
+        }
+        if (ik < iv && ik < ip && mbar_probe(bar(C::B_DSFULL), ik & 1)) {
+          tc_fence_after_sync();
+          const uint32_t q_s = sQ + (ik % C::NSTQ) * C::TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < C::BM / 16; ++kk)
+            mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
+                   (ik > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < C::BN / 16; ++kk) {
+            if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: both operands MN-major
+              mma_ss(tmem + C::T_DP, desc_mn_tile<D>(sK, kk), desc_ds_mnmajor(sDS, kk), id_dq,
+                     kk > 0 ? 1u : 0u);
+            else                    // dQ = dS K
+              mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
+                     kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bar(C::B_DQFULL));
+          tc_commit(bar(C::B_QEMPTY + ik % C::NSTQ));
+          tc_commit(bar(C::B_DSEMPTY));
+          ++ik;
           progress = true;
         }
         if (progress) {
