@@ -288,8 +288,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         IdleWatch watch;
         while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
           bool progress = false;
+          // Tile 1 is checked first: under the causal mask its chain is one key
+          // tile longer, and serving it first measured 1-5 % faster causal
+          // (no change without the mask).  Within a tile P V comes before S.
   #pragma unroll
-          for (int q = 0; q < 2; ++q) {
+          for (int qq = 0; qq < 2; ++qq) {
+            const int q = 1 - qq;
             // PV_q(jp).  With dropout it goes in two halves: keys 0-63 as soon
             // as the softmax has written that half of P (it draws and writes the
             // second half meanwhile), keys 64-127 once all of P_q is written.

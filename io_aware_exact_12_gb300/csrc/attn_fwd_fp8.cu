@@ -244,7 +244,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
         bool progress = false;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int qq = 0; qq < 2; ++qq) {  // tile 1 (the longer causal chain) first
+          const int q = 1 - qq;
           const int jv = jp[q];
           if (jv < nkv[q] && jv < js[q] &&
               mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
