@@ -203,6 +203,19 @@ def test_c5_very_long_sequence():
     _check_identities(x, grads)
 
 
+# The other compiled variants (fp16; d = 64 and 32) at a multi-wave size:
+# N = 4096 (32 key tiles), 16 heads, sampled rows and key columns.
+@pytest.mark.parametrize("dtype,d,causal", [("f16", 128, False), ("f16", 128, True), ("bf16", 64, False),
+                                            ("bf16", 64, True), ("bf16", 32, True), ("f16", 32, False)])
+def test_long_sequence_other_variants(dtype, d, causal):
+    x = make_inputs(AttnShape(2, 8, 4096, d), dtype, seed=12)
+    s = 1.0 / math.sqrt(d)
+    o, lse = gpu_fwd(x, s, causal)
+    grads = gpu_bwd(x, o, lse, s, causal)
+    _check_sampled(x, s, causal, o, lse, grads, nrows=256, heads_for_cols=[0, 15], ncols=32)
+    _check_identities(x, grads)
+
+
 # The causal kernels visit blocks heaviest first within groups of heads.  The
 # backward groups 32 MB / (8 N d bytes) heads: 4 at N = 8192, d = 128, so 10
 # heads make groups of 4, 4 and 2; the forward groups 128 MB / (4 N d bytes):
