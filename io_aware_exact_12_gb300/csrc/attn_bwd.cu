@@ -143,6 +143,14 @@ __device__ __forceinline__ uint64_t desc_ds_mnmajor(uint32_t tile, int kk) {
   return smem_desc(tile + kk * 16 * 128, 128 * 128, 1024, kSwizzle128B);
 }
 
+// Byte offset of 16-byte unit u of row `row` in the epilogue's staging copy of
+// a 128-row dK or dV tile (rows of 2 D = 256 bytes): the unit index is XOR-ed
+// with the row's low bits, so the row-per-thread writes and the row-contiguous
+// reads of a warp each touch eight bank groups per 8-lane phase.
+__device__ __forceinline__ uint32_t row_stage_off256(int row, int u) {
+  return static_cast<uint32_t>(row * 256 + ((u ^ (row & 7)) << 4));
+}
+
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_test(bar, parity)) {
@@ -557,13 +565,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       mbar_arrive(bar(C::B_DSFULL));
       if (DROP && it + 1 < nq) draw_visit(q0 + C::BM);
     }
-    // dK (warpgroup 0) or dV (warpgroup 1) once the last MMAs have completed
-    if (ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status)) {
+    // dK (warpgroup 0) or dV (warpgroup 1) once the last MMAs have completed.
+    // At d = 128 the rows leave through the K (dK) or V (dV) tile in shared
+    // memory, which no MMA reads any more: each thread writes its row there,
+    // then each warp stores its 32 rows with 512 contiguous bytes per
+    // instruction (as the forward's O).  The warp takes the branch together.
+    constexpr bool STAGE = (D == 128);
+    bool ep = ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status);
+    if constexpr (STAGE) ep = __all_sync(0xffffffffu, ep);
+    if (ep) {
       tc_fence_after_sync();
       const int64_t rbase = (static_cast<int64_t>(bh) * N + kv_row) * (D * 2);
       const uint32_t tcol = tmem + lane_off + (g == 0 ? C::T_DK : C::T_DV);
       const float mul = g == 0 ? scale : (DROP ? drop.rscale : 1.f);
-      uint8_t* dst_row = (g == 0 ? dk_out : dv_out) + rbase;
+      uint8_t* out = g == 0 ? dk_out : dv_out;
+      uint8_t* dst_row = out + rbase;
+      uint8_t* stage = smem + (g == 0 ? C::OFF_K : C::OFF_V);
 #pragma unroll
       for (int c0 = 0; c0 < D / 32; ++c0) {
         uint32_t v[32];
@@ -572,10 +589,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-        if (kv_row < N) {
+        if constexpr (STAGE) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(stage + row_stage_off256(t, c0 * 4 + i)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        } else if (kv_row < N) {
           uint4* dst = reinterpret_cast<uint4*>(dst_row + c0 * 64);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if constexpr (STAGE) {
+        __syncwarp();
+        const int wrow = t & ~31;  // this warp's first key row of the tile
+        uint8_t* obase = out + static_cast<int64_t>(bh) * N * (D * 2);
+#pragma unroll
+        for (int it = 0; it < 16; ++it) {
+          const int lin = it * 32 + lane;
+          const int rr = wrow + (lin >> 4), u = lin & 15;
+          const uint4 val = *reinterpret_cast<const uint4*>(stage + row_stage_off256(rr, u));
+          if (kv0 + rr < N) *reinterpret_cast<uint4*>(obase + static_cast<int64_t>(kv0 + rr) * (D * 2) + u * 16) = val;
         }
       }
     } else if (SPARSE && ok && nq == 0 && kv_row < N) {
