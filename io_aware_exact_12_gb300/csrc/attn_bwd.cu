@@ -174,7 +174,27 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(
   const int i = live ? static_cast<int>(rid % Npad) : 0;
   const bool real = live && i < N;
   float acc = 0.f;
-  if (real) {
+  if (real && D >= 64) {
+    // The row's 8 lanes take 16-byte pieces sub, sub + 8, ... so that each warp
+    // instruction reads (and zeroes) whole 128-byte runs of 4 rows.
+    const int64_t row_el = (bh * N + i) * D;
+    const uint4* po = reinterpret_cast<const uint4*>(o + row_el * 2);
+    const uint4* pd = reinterpret_cast<const uint4*>(dO + row_el * 2);
+#pragma unroll
+    for (int k = 0; k < D / 64; ++k) {
+      const uint4 a = po[sub + 8 * k], b = pd[sub + 8 * k];
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = unpack2<BF16>(aw[e]), y = unpack2<BF16>(bw[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+    float4* z = reinterpret_cast<float4*>(dq_acc + row_el);
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) z[sub + 8 * k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else if (real) {
     const int64_t off = (bh * N + i) * D + sub * PER;
     const uint32_t* po = reinterpret_cast<const uint32_t*>(o + off * 2);
     const uint32_t* pd = reinterpret_cast<const uint32_t*>(dO + off * 2);
