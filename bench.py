@@ -528,20 +528,21 @@ def run_ours(args):
     value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
     launches = K * 4
 
-    # causal variant of the same workload (reported alongside, not in `value`)
-    cf_ms, cb_ms = [], []
-    for _ in range(2):
+    # causal variant of the same workload (reported alongside, not in `value`),
+    # timed like the main step: back-to-back steps, one synchronisation at the end
+    for _ in range(3):
         step(True)
-    for _ in range(max(K // 2, 3)):
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize()
+    cev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(K // 2, 3))]
+    for e0, e1, e2 in cev:
         e0.record(stream)
         attn.attn_fwd(q, k, v, scale=scale, causal=True, o=o, lse=lse)
         e1.record(stream)
         attn.attn_bwd(q, k, v, o, do, lse, scale=scale, causal=True, dq=dq, dk=dk, dv=dv)
         e2.record(stream)
-        torch.cuda.synchronize()
-        cf_ms.append(e0.elapsed_time(e1))
-        cb_ms.append(e1.elapsed_time(e2))
+    torch.cuda.synchronize()
+    cf_ms = [e0.elapsed_time(e1) for e0, e1, _ in cev]
+    cb_ms = [e1.elapsed_time(e2) for _, e1, e2 in cev]
     cf_f, cb_f = flops_per_step(B, H, N, d, True)
 
     # end to end through the public API: pinned host inputs -> device -> fwd+bwd -> host outputs
