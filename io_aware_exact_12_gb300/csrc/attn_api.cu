@@ -4,6 +4,7 @@
 // attn_fwd.cu / attn_bwd.cu; this file only checks and marshals.
 #include <cmath>
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -164,6 +165,27 @@ bool check_launch_regs(const void* func, int regs) {
   return fa.numRegs == regs;
 }
 
+int device_sm_count() {
+  static std::atomic<int> count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = count[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+  count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int bwd_tail_split(int BH, int N, int causal) {
+  if (causal) return 0;
+  const int64_t ntq = (static_cast<int64_t>(N) + 127) / 128;
+  if (ntq < 2) return 0;  // a key tile with one query tile has nothing to split
+  const int sms = device_sm_count();
+  if (sms <= 0) return 0;
+  const int64_t r = (ntq * BH) % sms;
+  return (r > 0 && 2 * r <= sms) ? static_cast<int>(r) : 0;
+}
+
 int* status_word_current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -261,9 +283,11 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   int* st = status_ptr(dev);
   if (!st) return kStatusCuda;
   const BwdScratch lay = bwd_scratch_layout(B * H, N, d);
+  const int tail = bmask ? 0 : bwd_tail_split(B * H, N, causal);
+  const size_t part_bytes = static_cast<size_t>(tail) * 4 * 128 * d * sizeof(float);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, lay.total, s) != cudaSuccess) return kStatusCuda;
+  if (cudaMallocAsync(&ws, lay.total + part_bytes, s) != cudaSuccess) return kStatusCuda;
   BwdArgs a;
   a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse;
   a.dq = dq; a.dk = dk; a.dv = dv;
@@ -282,6 +306,8 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
   a.bmask = bmask;
   a.H = H;
   a.mask_heads = mask_heads;
+  a.tail_split = tail;
+  a.ws_part = tail ? reinterpret_cast<float*>(static_cast<char*>(ws) + lay.total) : nullptr;
   rc = launch_bwd(a);
   const cudaError_t fe = cudaFreeAsync(ws, s);
   if (rc == kStatusOk && fe != cudaSuccess) rc = kStatusCuda;

@@ -222,16 +222,46 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(
 }
 
 // ---------------------------------------------------------------- convert
-template <bool BF16>
+// fp32 dQ accumulator -> dQ; then, for the key tiles whose query range was
+// split over two CTAs (the grid's last partial wave, see launch_bwd_t), dK and
+// dV = the sum of the two CTAs' fp32 partial tiles.  part holds, per split
+// tile s, half h and output (0 = dK, 1 = dV), a 128 x D fp32 tile:
+// part[((s * 2 + h) * 2 + out) * 128 * D + row * D + col].
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256) attn_dq_convert_kernel(const float* __restrict__ acc,
                                                               uint8_t* __restrict__ dq,
-                                                              int64_t groups) {
-  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups;
-       g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+                                                              int64_t groups,
+                                                              const float* __restrict__ part, int nsplit,
+                                                              int split_from, int nkt, int N,
+                                                              uint8_t* __restrict__ dk,
+                                                              uint8_t* __restrict__ dv) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t g = tid; g < groups; g += stride) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * g];
     const float4 b = reinterpret_cast<const float4*>(acc)[2 * g + 1];
     reinterpret_cast<uint4*>(dq)[g] = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w),
                                                  pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
+  }
+  // combine: 8 consecutive columns of one row of one output per step
+  constexpr int G = D / 8;  // 8-column groups per row
+  const int64_t cgroups = static_cast<int64_t>(nsplit) * 2 * 128 * G;
+  for (int64_t g = tid; g < cgroups; g += stride) {
+    const int c8 = static_cast<int>(g % G);
+    const int row = static_cast<int>((g / G) % 128);
+    const int out = static_cast<int>((g / (G * 128)) % 2);
+    const int sidx = static_cast<int>(g / (G * 128 * 2));
+    const int item = split_from + sidx;  // the split tile's block index before splitting
+    const int jt = item % nkt, bh = item / nkt;
+    const int kv_row = jt * 128 + row;
+    if (kv_row >= N) continue;
+    const float* p0 = part + ((static_cast<int64_t>(sidx) * 2 + 0) * 2 + out) * 128 * D + row * D + c8 * 8;
+    const float* p1 = part + ((static_cast<int64_t>(sidx) * 2 + 1) * 2 + out) * 128 * D + row * D + c8 * 8;
+    const float4 a0 = reinterpret_cast<const float4*>(p0)[0], a1 = reinterpret_cast<const float4*>(p0)[1];
+    const float4 b0 = reinterpret_cast<const float4*>(p1)[0], b1 = reinterpret_cast<const float4*>(p1)[1];
+    uint8_t* dst = (out == 0 ? dk : dv) + ((static_cast<int64_t>(bh) * N + kv_row) * D + c8 * 8) * 2;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pack2<BF16>(a0.x + b0.x, a0.y + b0.y), pack2<BF16>(a0.z + b0.z, a0.w + b0.w),
+                                                pack2<BF16>(a1.x + b1.x, a1.y + b1.y), pack2<BF16>(a1.z + b1.z, a1.w + b1.w));
   }
 }
 
@@ -260,17 +290,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     uint8_t* __restrict__ dk_out, uint8_t* __restrict__ dv_out, int N, int Npad,
                     float sl2, float scale, int causal, int negate, int* status,
                     DropParams drop, const uint8_t* __restrict__ bmask, int H, int mask_heads,
-                    int head_group) {
+                    int head_group, int BH, int split_from, float* __restrict__ part) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int jt = blockIdx.x, bh = blockIdx.y;  // key tile, head
-  if (causal)  // key tile 0 sees every query tile: heaviest (of a group of heads) first
-    grouped_rank_order(blockIdx.x + blockIdx.y * gridDim.x, gridDim.x, gridDim.y, head_group, jt, bh);
-  const int kv0 = jt * C::BN;
+  const int nkt = (N + C::BN - 1) / C::BN;
   const int ntq = (N + C::BM - 1) / C::BM;
-  const int i0 = causal ? jt : 0;
+  // One-dimensional grid over (key tile, head) items.  Blocks from split_from
+  // on come in pairs: the two halves of one item's query range (the grid's
+  // last partial wave, split so that it takes half a wave; dK and dV then go
+  // out as fp32 partial tiles that attn_dq_convert_kernel adds).
+  int item = blockIdx.x, half = -1, sidx = 0;
+  if (item >= split_from) {
+    sidx = (item - split_from) >> 1;
+    half = (item - split_from) & 1;
+    item = split_from + sidx;
+  }
+  int jt, bh;  // key tile, head
+  if (causal) {  // key tile 0 sees every query tile: heaviest (of a group of heads) first
+    grouped_rank_order(item, nkt, BH, head_group, jt, bh);
+  } else {
+    bh = item / nkt;
+    jt = item - bh * nkt;
+  }
+  const int kv0 = jt * C::BN;
+  // query tiles [i0, i0 + nq_dense): from the diagonal under the causal mask,
+  // else all of them, or one half of them for a split item
+  int i0 = causal ? jt : 0;
+  int nq_dense = ntq - i0;
+  if (half >= 0) {
+    i0 = half == 0 ? 0 : ntq / 2;
+    nq_dense = half == 0 ? ntq / 2 : ntq - ntq / 2;
+  }
 
   const uint32_t sbase = smem_addr(smem);
   if (sbase & 1023u) {
@@ -321,7 +373,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  const int nq = SPARSE ? *qcount : ntq - i0;  // query tiles this key tile visits
+  const int nq = SPARSE ? *qcount : nq_dense;  // query tiles this key tile visits
   // Query tile of visit `it`: i0 + it, or (SPARSE) the next set bit after the
   // cursor `qi` of the previous visit (start qi = i0 - 1).  The dense form is
   // kept as a plain expression: the cursor form measured 4 % slower there.
@@ -593,7 +645,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     constexpr bool STAGE = (D == 128);
     bool ep = ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status);
     if constexpr (STAGE) ep = __all_sync(0xffffffffu, ep);
-    if (ep) {
+    if (ep && half >= 0) {
+      // a split item: this half's fp32 tile (x scale for dK, x 256/t for dV)
+      tc_fence_after_sync();
+      const uint32_t tcol = tmem + lane_off + (g == 0 ? C::T_DK : C::T_DV);
+      const float mul = g == 0 ? scale : (DROP ? drop.rscale : 1.f);
+      float4* prow = reinterpret_cast<float4*>(part + ((static_cast<int64_t>(sidx) * 2 + half) * 2 + g) * 128 * D +
+                                               static_cast<int64_t>(t) * D);
+#pragma unroll
+      for (int c0 = 0; c0 < D / 32; ++c0) {
+        uint32_t v[32];
+        tmem_ld32(tcol + c0 * 32, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          prow[c0 * 8 + i] = make_float4(__uint_as_float(v[4 * i]) * mul, __uint_as_float(v[4 * i + 1]) * mul,
+                                         __uint_as_float(v[4 * i + 2]) * mul, __uint_as_float(v[4 * i + 3]) * mul);
+      }
+    } else if (ep) {
       tc_fence_after_sync();
       const int64_t rbase = (static_cast<int64_t>(bh) * N + kv_row) * (D * 2);
       const uint32_t tcol = tmem + lane_off + (g == 0 ? C::T_DK : C::T_DV);
@@ -711,16 +779,24 @@ int launch_bwd_t(const BwdArgs& a) {
         static_cast<const uint8_t*>(a.o), static_cast<const uint8_t*>(a.dO), a.lse, a.ws_lse2,
         a.ws_d, a.ws_dq, a.N, Npad, rows_total);
   }
-  dim3 grid((a.N + C::BN - 1) / C::BN, a.BH);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(
+  // One block per (key tile, head) item, head after head; the last tail_split
+  // items (no causal mask, no block mask) as two half-range blocks each.
+  const int nkt = (a.N + C::BN - 1) / C::BN;
+  const int64_t items = static_cast<int64_t>(nkt) * a.BH;
+  const int tail = (SPARSE || a.causal || !a.ws_part) ? 0 : a.tail_split;
+  if (items + tail > 0x7fffffff) return kStatusUnsupported;
+  const int split_from = static_cast<int>(items - tail);
+  kern<<<static_cast<unsigned>(items + tail), C::THREADS, C::SMEM_BYTES, a.stream>>>(
       mq, mk, mv, mdo, a.ws_lse2, a.ws_d, a.ws_dq, static_cast<uint8_t*>(a.dk),
       static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status, a.drop,
-      a.bmask, a.H, a.mask_heads, order_head_group(a.BH, int64_t{8} * a.N * D, int64_t{32} << 20));
+      a.bmask, a.H, a.mask_heads, order_head_group(a.BH, int64_t{8} * a.N * D, int64_t{32} << 20), a.BH,
+      split_from, a.ws_part);
   {
     const int64_t groups = static_cast<int64_t>(a.BH) * a.N * D / 8;
     const int blocks = static_cast<int>(std::min<int64_t>((groups + 255) / 256, 152 * 16));
-    attn_dq_convert_kernel<BF16><<<blocks, 256, 0, a.stream>>>(a.ws_dq,
-                                                               static_cast<uint8_t*>(a.dq), groups);
+    attn_dq_convert_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(
+        a.ws_dq, static_cast<uint8_t*>(a.dq), groups, a.ws_part, tail, split_from, nkt, a.N,
+        static_cast<uint8_t*>(a.dk), static_cast<uint8_t*>(a.dv));
   }
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }

@@ -73,7 +73,19 @@ struct BwdArgs {
   const uint8_t* bmask = nullptr;
   int H = 1;
   int mask_heads = 1;
+  // Split of the grid's last partial wave (0 = none; see bwd_tail_split): the
+  // last tail_split (key tile, head) items each run as two CTAs over half of
+  // the query tiles, writing fp32 partial dK/dV tiles to ws_part
+  // (tail_split * 2 halves * 2 outputs * 128 * d floats).
+  int tail_split = 0;
+  float* ws_part = nullptr;
 };
+
+// Items of the backward's last partial wave to split in two, or 0: without
+// the causal mask (equal work per item) W = ceil(N/128) * BH items fill W / S
+// full waves of the S SMs plus r = W mod S; when 2 r <= S the r items run as
+// 2 r half-length CTAs, finishing in half a wave.
+int bwd_tail_split(int BH, int N, int causal);
 
 // Bytes of backward scratch for a problem, and its carve-up.
 struct BwdScratch {
@@ -92,6 +104,10 @@ bool ensure_smem_attr(const void* func, int bytes);
 // True iff the kernel was built with exactly `regs` registers per thread (a
 // warpgroup register split that does not add up would wait forever).
 bool check_launch_regs(const void* func, int regs);
+
+// Streaming multiprocessors of the current device (looked up once per device);
+// 0 on error.
+int device_sm_count();
 
 struct DecodeArgs {
   const void *q, *k, *v;  // q [BH][d], k/v [BH][L][d] bf16
