@@ -12,8 +12,13 @@
 //                              and zeroes the fp32 dQ accumulator.
 //   2. attn_bwd_kernel       : one CTA per (128-key tile, head), the key tile
 //                              stays in shared memory and dK/dV accumulate in
-//                              TMEM over every query tile that can see it.
-//   3. attn_dq_convert_kernel: fp32 dQ accumulator -> bf16/fp16 dQ.
+//                              TMEM over every query tile that can see it
+//                              (without the causal mask, a last partial wave of
+//                              at most half the SMs runs each of its tiles as
+//                              two CTAs over half of the query tiles, writing
+//                              fp32 partial dK/dV).
+//   3. attn_dq_convert_kernel: fp32 dQ accumulator -> bf16/fp16 dQ, and the
+//                              split tiles' dK/dV = sum of their two partials.
 //
 // attn_bwd_kernel roles (16 warps = 4 warpgroups, one CTA per SM; warpgroup 3
 // hands registers to warpgroups 0-2 with setmaxnreg: 152, 152, 144 / 64):
