@@ -79,10 +79,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *                    D_i = sum_k dO_ik O_ik, dS = P o (dO V^T - D),
  *                    dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
  * Recomputation: FlashAttention (PKM page) "三招" 3; FlashAttention深度攻略 §6.
- * Scratch: an fp32 dQ accumulator [B, H, N, d] and D [B, H, N] are taken
- * from the stream-ordered allocator (cudaMallocAsync on `stream`) and freed
- * on the same stream before the call returns (the memory is released when
- * the stream reaches that point).
+ * Scratch: an fp32 dQ accumulator [B, H, N, d] and D [B, H, N] (plus, when
+ * a non-causal grid's last partial wave is split over query halves, at most
+ * (SMs / 2) x 4 fp32 128 x d tiles of partial dK/dV) are taken from the
+ * stream-ordered allocator (cudaMallocAsync on `stream`) and freed on the
+ * same stream before the call returns (the memory is released when the
+ * stream reaches that point).
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
              const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
