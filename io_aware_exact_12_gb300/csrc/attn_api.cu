@@ -180,10 +180,7 @@ int bwd_tail_split(int BH, int N, int causal) {
   if (causal) return 0;
   const int64_t ntq = (static_cast<int64_t>(N) + 127) / 128;
   if (ntq < 2) return 0;  // a key tile with one query tile has nothing to split
-  const int sms = device_sm_count();
-  if (sms <= 0) return 0;
-  const int64_t r = (ntq * BH) % sms;
-  return (r > 0 && 2 * r <= sms) ? static_cast<int>(r) : 0;
+  return tail_split_items(ntq * BH, device_sm_count());
 }
 
 int* status_word_current_device() {

@@ -306,12 +306,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   // on come in pairs: the two halves of one item's query range (the grid's
   // last partial wave, split so that it takes half a wave; dK and dV then go
   // out as fp32 partial tiles that attn_dq_convert_kernel adds).
-  int item = blockIdx.x, half = -1, sidx = 0;
-  if (item >= split_from) {
-    sidx = (item - split_from) >> 1;
-    half = (item - split_from) & 1;
-    item = split_from + sidx;
-  }
+  int item, half;
+  split_block_item(static_cast<int>(blockIdx.x), split_from, item, half);
+  const int sidx = item - split_from;  // index of a split item's partial tiles
   int jt, bh;  // key tile, head
   if (causal) {  // key tile 0 sees every query tile: heaviest (of a group of heads) first
     grouped_rank_order(item, nkt, BH, head_group, jt, bh);

@@ -82,9 +82,8 @@ struct BwdArgs {
 };
 
 // Items of the backward's last partial wave to split in two, or 0: without
-// the causal mask (equal work per item) W = ceil(N/128) * BH items fill W / S
-// full waves of the S SMs plus r = W mod S; when 2 r <= S the r items run as
-// 2 r half-length CTAs, finishing in half a wave.
+// the causal mask every (key tile, head) item costs the same, so
+// tail_split_items(ceil(N/128) * BH, SMs) of block_order.h applies.
 int bwd_tail_split(int BH, int N, int causal);
 
 // Bytes of backward scratch for a problem, and its carve-up.

@@ -41,4 +41,29 @@ inline int order_head_group(int BH, int64_t bytes_per_head, int64_t budget) {
   return static_cast<int>(g);
 }
 
+// Split of a grid's last partial wave.  W equal-cost items on S SMs run as
+// W / S full waves plus a last wave of r = W mod S items while S - r SMs idle;
+// when 2 r <= S, those r items can each run as two blocks over half of the
+// item's range, so the last wave takes half as long.  Returns how many items
+// to split (0: none).
+__host__ __device__ inline int tail_split_items(int64_t W, int S) {
+  if (W <= 0 || S <= 0) return 0;
+  const int64_t r = W % S;
+  return (r > 0 && 2 * r <= S) ? static_cast<int>(r) : 0;
+}
+
+// Block b of a grid of W + r blocks whose last r items are split (split_from =
+// W - r): the item it works on, and which half of the item's range (-1: all).
+// Blocks below split_from map one to one; from there on, blocks come in pairs
+// (half 0, half 1) of consecutive items.
+__host__ __device__ inline void split_block_item(int b, int split_from, int& item, int& half) {
+  if (b < split_from) {
+    item = b;
+    half = -1;
+  } else {
+    item = split_from + ((b - split_from) >> 1);
+    half = (b - split_from) & 1;
+  }
+}
+
 }  // namespace attn

@@ -1,8 +1,13 @@
-// Host check of the causal kernels' block order (grouped_rank_order,
-// order_head_group in block_order.h): for every grid of nblk x BH blocks
-// and every head-group size, the linear block indices map one-to-one onto
-// (rank, head) pairs, ranks run heaviest-first within a group, and a group
-// holds at most g heads.  Prints "ok" and exits 0 when every case holds.
+// Host check of the block-order helpers in block_order.h:
+//  - grouped_rank_order / order_head_group (the causal kernels' order): for
+//    every grid of nblk x BH blocks and every head-group size, the linear block
+//    indices map one-to-one onto (rank, head) pairs, ranks run heaviest-first
+//    within a group, and a group holds at most g heads;
+//  - tail_split_items / split_block_item (the backward's split last wave):
+//    the split items are exactly the last partial wave when it is at most half
+//    the SMs, and the grid's blocks cover every unsplit item once and both
+//    halves of every split item.
+// Prints "ok" and exits 0 when every case holds.
 #include <cstdio>
 #include <vector>
 
@@ -50,6 +55,46 @@ int main() {
       attn::order_head_group(4, 1, int64_t{32} << 20) != 4) {
     std::printf("order_head_group\n");
     return 1;
+  }
+  // tail split: which items of a grid's last partial wave run as two halves
+  for (int S : {1, 7, 148, 152}) {
+    for (int64_t W = 1; W <= 3000; W += (W < 400 ? 1 : 7)) {
+      const int r = attn::tail_split_items(W, S);
+      const int64_t rem = W % S;
+      if (r > 0) {
+        if (r != rem || 2 * r > S || (W - r) % S != 0) {
+          std::printf("tail split: W=%lld S=%d r=%d\n", static_cast<long long>(W), S, r);
+          return 1;
+        }
+      } else if (rem != 0 && 2 * rem <= S) {
+        std::printf("tail split missed: W=%lld S=%d\n", static_cast<long long>(W), S);
+        return 1;
+      }
+      // blocks -> (item, half): unsplit items once, split items once per half
+      const int split_from = static_cast<int>(W - r);
+      std::vector<int> whole(static_cast<size_t>(W), 0), halves(static_cast<size_t>(W), 0);
+      for (int b = 0; b < W + r; ++b) {
+        int item = -1, half = -2;
+        attn::split_block_item(b, split_from, item, half);
+        if (item < 0 || item >= W || (half == -1) != (item < split_from) || half < -1 || half > 1) {
+          std::printf("split mapping: W=%lld r=%d b=%d -> item=%d half=%d\n", static_cast<long long>(W), r, b,
+                      item, half);
+          return 1;
+        }
+        if (half < 0) ++whole[static_cast<size_t>(item)];
+        else halves[static_cast<size_t>(item)] |= 1 << half;
+      }
+      for (int64_t i = 0; i < W; ++i) {
+        const bool ok = i < split_from ? (whole[static_cast<size_t>(i)] == 1 && halves[static_cast<size_t>(i)] == 0)
+                                       : (whole[static_cast<size_t>(i)] == 0 && halves[static_cast<size_t>(i)] == 3);
+        if (!ok) {
+          std::printf("split coverage: W=%lld r=%d item=%lld\n", static_cast<long long>(W), r,
+                      static_cast<long long>(i));
+          return 1;
+        }
+      }
+      ++cases;
+    }
   }
   std::printf("%d grids ok\n", cases);
   return 0;

@@ -1,15 +1,15 @@
-"""The causal kernels visit (block, head) pairs in a grouped heaviest-first
-order computed on the device from the linear block index.  This builds the
-same header function for the host (tests/block_order_check.cpp) and checks
-that it is a bijection onto every (rank, head) pair for many grid shapes and
-head-group sizes, with ranks non-decreasing within a group."""
+"""The kernels' block-order helpers (block_order.h), built for the host by
+tests/block_order_check.cpp: the causal kernels' grouped heaviest-first order
+is a bijection onto every (rank, head) pair with ranks non-decreasing within a
+group, and the backward's split of its last partial wave covers every item
+(the split ones by both halves) for many grid and SM counts."""
 import os
 import subprocess
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_grouped_rank_order_is_a_bijection(tmp_path):
+def test_block_order_helpers(tmp_path):
     exe = str(tmp_path / "block_order_check")
     cmd = ["g++", "-std=c++17", "-O1", "-Wall", "-I", os.path.join(ROOT, "io_aware_exact_12_gb300", "csrc"),
            os.path.join(ROOT, "tests", "block_order_check.cpp"), "-o", exe]
