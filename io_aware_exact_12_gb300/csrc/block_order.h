@@ -53,16 +53,18 @@ __host__ __device__ inline int tail_split_items(int64_t W, int S) {
 }
 
 // Block b of a grid of W + r blocks whose last r items are split (split_from =
-// W - r): the item it works on, and which half of the item's range (-1: all).
-// Blocks below split_from map one to one; from there on, blocks come in pairs
-// (half 0, half 1) of consecutive items.
-__host__ __device__ inline void split_block_item(int b, int split_from, int& item, int& half) {
-  if (b < split_from) {
-    item = b;
-    half = -1;
-  } else {
-    item = split_from + ((b - split_from) >> 1);
+// W - r): the item it works on, which half of the item's range (-1: all) and,
+// for a split item, its pair index item - split_from.  Blocks below
+// split_from map one to one; from there on, blocks come in pairs (half 0,
+// half 1) of consecutive items.
+__host__ __device__ inline void split_block_item(int b, int split_from, int& item, int& half, int& pair) {
+  item = b;
+  half = -1;
+  pair = 0;  // index of the split pair (0 for blocks below split_from)
+  if (b >= split_from) {
+    pair = (b - split_from) >> 1;
     half = (b - split_from) & 1;
+    item = split_from + pair;
   }
 }
 

@@ -74,9 +74,10 @@ int main() {
       const int split_from = static_cast<int>(W - r);
       std::vector<int> whole(static_cast<size_t>(W), 0), halves(static_cast<size_t>(W), 0);
       for (int b = 0; b < W + r; ++b) {
-        int item = -1, half = -2;
-        attn::split_block_item(b, split_from, item, half);
-        if (item < 0 || item >= W || (half == -1) != (item < split_from) || half < -1 || half > 1) {
+        int item = -1, half = -2, pair = -1;
+        attn::split_block_item(b, split_from, item, half, pair);
+        if (item < 0 || item >= W || (half == -1) != (item < split_from) || half < -1 || half > 1 ||
+            pair != (half < 0 ? 0 : item - split_from)) {
           std::printf("split mapping: W=%lld r=%d b=%d -> item=%d half=%d\n", static_cast<long long>(W), r, b,
                       item, half);
           return 1;
