@@ -29,7 +29,10 @@
 //               as bf16/fp16 over the first half of its S columns.  l is kept
 //               twice: the exact sum for LSE, and the sum of the rounded P
 //               values (the weights actually applied to V) to normalise O.
-//   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+//   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
+//     at d <= 64 also P0, P1 (64 columns each) after O1, so a tile's next S
+//     goes out once its softmax has read the current S instead of after the
+//     current P V has finished; at d = 128 P_q overwrites half of S_q.
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied; only the diagonal tile (and the ragged last tile) are masked;
 // the CTAs run heaviest first across a group of heads (block_order.h).
@@ -77,7 +80,8 @@ struct FwdCfg {
   static constexpr int B_ODONE = B_PFULL + 2;
   static constexpr int B_MMADONE = B_ODONE + 2;
   static constexpr int B_PHALF = B_MMADONE + 1;  // dropout: first 64 keys of P_q written
-  static constexpr int NBAR = B_PHALF + 2;
+  static constexpr int B_STAKEN = B_PHALF + 2;   // SEPP: S_q read into registers
+  static constexpr int NBAR = B_STAKEN + 2;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int OFF_NPOS = OFF_ABORT + 4;                   // int[3]: positions, per-tile counts
@@ -90,7 +94,16 @@ struct FwdCfg {
   static constexpr int REGS_CTRL = 56;      // producer / MMA warpgroup
   static_assert(2 * 128 * REGS_MATH + 128 * REGS_CTRL <= THREADS * REGS_LAUNCH, "register split");
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(2 * 128 + 2 * D <= 512, "TMEM budget");
+  // At d <= 64, P_q has TMEM columns of its own after O0, O1 (64 columns of
+  // packed 16-bit values each), so S_q(j+1) can be computed as soon as the
+  // softmax has read S_q(j), while P_q(j) V_j is still pending.  At d = 128
+  // the 512 columns are full and P_q overwrites the first half of S_q.
+  static constexpr bool SEPP = (D <= 64);
+  static constexpr uint32_t TM_S = 0;                            // + 128 q
+  static constexpr uint32_t TM_O = 2 * BN;                       // + D q
+  static constexpr uint32_t TM_P = SEPP ? 2 * BN + 2 * D : 0;    // + (SEPP ? 64 : 128) q
+  static constexpr uint32_t TM_PSTRIDE = SEPP ? BN / 2 : BN;
+  static_assert(2 * 128 + 2 * D + (SEPP ? 2 * 64 : 0) <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -109,6 +122,19 @@ template <int D>
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   using C = FwdCfg<D>;
   return smem_desc(tile + kk * 16 * C::ROWB, C::CHUNK_BYTES, C::SBO, C::SWZ);
+}
+
+// The same two descriptors as words (smem_desc_lo/hi): the issuers form the
+// low word of a tile once per MMA group and add these per-slice offsets, so
+// each MMA costs one add per operand.
+template <int D>
+__host__ __device__ constexpr uint32_t kmajor_lo_step(int kk) {
+  using C = FwdCfg<D>;
+  return static_cast<uint32_t>(((kk * 16) / C::CH * C::CHUNK_BYTES + (kk * 16) % C::CH * 2) >> 4);
+}
+template <int D>
+__host__ __device__ constexpr uint32_t mnmajor_lo_step(int kk) {
+  return static_cast<uint32_t>((kk * 16 * FwdCfg<D>::ROWB) >> 4);
 }
 
 // Byte offset of 16-byte unit u of row `row` in the epilogue's staging copy of
@@ -199,15 +225,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 2);  // one unit per query tile (see the softmax)
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), SPARSE ? 1 : 2);  // block-sparse: the issuer releases V
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar(C::B_SFULL + q), 1);
       mbar_init(bar(C::B_PFULL + q), C::BM);
       mbar_init(bar(C::B_PHALF + q), C::BM);
       mbar_init(bar(C::B_ODONE + q), 1);
+      mbar_init(bar(C::B_STAKEN + q), C::BM);
     }
     mbar_init(bar(C::B_MMADONE), 1);
     *abort_flag = 0;
@@ -285,7 +312,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       //   S_q at position p  needs K_p resident and the tile's previous PV
       //                      complete (P_q aliases S_q);
       //   PV_q at position p needs V_p resident and P_q written by the softmax.
-      // A K (V) stage is released once both tiles are past its position.
+      // The K and V stages are released by the softmax threads (below), which
+      // learn from their own waits when the MMAs reading a stage have
+      // completed: the issuer's only tcgen05 operations are the MMAs and one
+      // commit per group.  (The issuing thread shares its SM sub-partition with
+      // two softmax warps, so each instruction it saves shortens the chain.)
+      constexpr uint32_t HI = smem_desc_hi(C::SBO, C::SWZ);
+      const uint32_t q_lo0 = smem_desc_lo(sQ, 16), q_lo1 = smem_desc_lo(sQ + C::TILE_BYTES, 16);
       if constexpr (!SPARSE) {
         const uint32_t idesc_s = instr_desc_f16(C::BM, C::BN, BF16, false, false, negate != 0);
         const uint32_t idesc_o = instr_desc_f16(C::BM, D, BF16, false, true);
@@ -294,7 +327,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         int js[2] = {0, 0};  // next S index per tile
         int jp[2] = {0, 0};  // next PV index per tile
         bool half[2] = {false, false};  // first half of PV_q(jp) issued
-        int k_rel = 0, v_rel = 0;  // next key/value tile whose stage is still held
         IdleWatch watch;
         while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
           bool progress = false;
@@ -314,13 +346,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                 mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
                 mbar_probe(bar((DROP ? C::B_PHALF : C::B_PFULL) + q), jv & 1)) {
               tc_fence_after_sync();
-              const uint32_t d_o = tmem + 2 * C::BN + q * D;
-              const uint32_t a_p = tmem + q * C::BN;
-              const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+              const uint32_t d_o = tmem + C::TM_O + q * D;
+              const uint32_t a_p = tmem + C::TM_P + q * C::TM_PSTRIDE;
+              const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, C::CHUNK_BYTES);
               constexpr int KK_FIRST = DROP ? C::BN / 32 : C::BN / 16;
   #pragma unroll
               for (int kk = 0; kk < KK_FIRST; ++kk)
-                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_w(d_o, a_p + kk * 8, v_lo + mnmajor_lo_step<D>(kk), HI, idesc_o, (jv > 0 || kk > 0) ? 1u : 0u);
               if constexpr (DROP) {
                 half[q] = true;
               } else {
@@ -331,42 +363,37 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             if (DROP && half[q] && mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
               tc_fence_after_sync();
-              const uint32_t d_o = tmem + 2 * C::BN + q * D;
-              const uint32_t a_p = tmem + q * C::BN;
-              const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+              const uint32_t d_o = tmem + C::TM_O + q * D;
+              const uint32_t a_p = tmem + C::TM_P + q * C::TM_PSTRIDE;
+              const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, C::CHUNK_BYTES);
   #pragma unroll
               for (int kk = C::BN / 32; kk < C::BN / 16; ++kk)
-                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, 1u);
+                mma_ts_w(d_o, a_p + kk * 8, v_lo + mnmajor_lo_step<D>(kk), HI, idesc_o, 1u);
               tc_commit(bar(C::B_ODONE + q));
               jp[q] = jv + 1;
               half[q] = false;
               progress = true;
             }
-            // S_q(js)
+            // S_q(js).  With P in S's columns (d = 128) it needs the tile's
+            // previous P V complete; with P apart (SEPP) only the previous S
+            // read out by the softmax.
             const int jk = js[q];
-            if (jk < nkv[q] && jk == jp[q] &&
+            if (jk < nkv[q] && (C::SEPP || jk == jp[q]) &&
                 mbar_probe(bar(C::B_KFULL + jk % C::NST), (jk / C::NST) & 1) &&
-                (jk == 0 || mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1))) {
+                (jk == 0 || (C::SEPP ? mbar_probe(bar(C::B_STAKEN + q), (jk - 1) & 1)
+                                     : mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1)))) {
               tc_fence_after_sync();
-              const uint32_t d_s = tmem + q * C::BN;
-              const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
+              const uint32_t d_s = tmem + C::TM_S + q * C::BN;
+              const uint32_t a_lo = q ? q_lo1 : q_lo0;
+              const uint32_t k_lo = smem_desc_lo(sK + (jk % C::NST) * C::TILE_BYTES, 16);
   #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
-                       kk > 0 ? 1u : 0u);
+                mma_ss_w(d_s, a_lo + kmajor_lo_step<D>(kk), HI, k_lo + kmajor_lo_step<D>(kk), HI, idesc_s,
+                         kk > 0 ? 1u : 0u);
               tc_commit(bar(C::B_SFULL + q));
               js[q] = jk + 1;
               progress = true;
             }
-          }
-          // release stages both tiles are done issuing from
-          while (k_rel < nkv_max && (js[0] > k_rel || k_rel >= nkv[0]) && (js[1] > k_rel || k_rel >= nkv[1])) {
-            tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
-            ++k_rel;
-          }
-          while (v_rel < nkv_max && (jp[0] > v_rel || v_rel >= nkv[0]) && (jp[1] > v_rel || v_rel >= nkv[1])) {
-            tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
-            ++v_rel;
           }
           if (progress) {
             watch.progress();
@@ -382,10 +409,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         int sp[2] = {0, 0};  // next position to consider for S, per tile
         int pp[2] = {0, 0};  // next position to consider for PV, per tile
         int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
-        int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
         int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
+        int v_rel = 0;                 // next position whose V stage is still held
         IdleWatch watch;
-        while (ok && (k_rel < npos || v_rel < npos)) {
+        while (ok && (np[0] < cnt[0] || np[1] < cnt[1] || v_rel < npos)) {
           bool progress = false;
           // Loads are observed strictly in position order: when position p is
           // probed, every earlier load on its stage has been seen, so the stage
@@ -403,12 +430,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             const int jv = pp[q];
             if (jv < sp[q] && jv < v_ready && mbar_probe(bar(C::B_PFULL + q), np[q] & 1)) {
               tc_fence_after_sync();
-              const uint32_t d_o = tmem + 2 * C::BN + q * D;
-              const uint32_t a_p = tmem + q * C::BN;
-              const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+              const uint32_t d_o = tmem + C::TM_O + q * D;
+              const uint32_t a_p = tmem + C::TM_P + q * C::TM_PSTRIDE;
+              const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, C::CHUNK_BYTES);
   #pragma unroll
               for (int kk = 0; kk < C::BN / 16; ++kk)
-                mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (np[q] > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_w(d_o, a_p + kk * 8, v_lo + mnmajor_lo_step<D>(kk), HI, idesc_o,
+                         (np[q] > 0 || kk > 0) ? 1u : 0u);
               tc_commit(bar(C::B_ODONE + q));
               pp[q] = jv + 1;
               ++np[q];
@@ -416,26 +444,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
             // S_q at sp
             const int jk = sp[q];
-            if (jk < npos && ns[q] == np[q] && jk < k_ready &&
-                (ns[q] == 0 || mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1))) {
+            if (jk < npos && (C::SEPP || ns[q] == np[q]) && jk < k_ready &&
+                (ns[q] == 0 || (C::SEPP ? mbar_probe(bar(C::B_STAKEN + q), (ns[q] - 1) & 1)
+                                        : mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1)))) {
               tc_fence_after_sync();
-              const uint32_t d_s = tmem + q * C::BN;
-              const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
+              const uint32_t d_s = tmem + C::TM_S + q * C::BN;
+              const uint32_t a_lo = q ? q_lo1 : q_lo0;
+              const uint32_t k_lo = smem_desc_lo(sK + (jk % C::NST) * C::TILE_BYTES, 16);
   #pragma unroll
               for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
-                       kk > 0 ? 1u : 0u);
+                mma_ss_w(d_s, a_lo + kmajor_lo_step<D>(kk), HI, k_lo + kmajor_lo_step<D>(kk), HI, idesc_s,
+                         kk > 0 ? 1u : 0u);
               tc_commit(bar(C::B_SFULL + q));
               sp[q] = jk + 1;
               ++ns[q];
               progress = true;
             }
           }
-          // release stages both tiles are past
-          while (k_rel < npos && sp[0] > k_rel && sp[1] > k_rel) {
-            tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
-            ++k_rel;
-          }
+          // A tile holds a position's V until its P V completes; under a block
+          // mask its next position may lie beyond the ring, so the softmax
+          // cannot release V from its next step's wait (the load it needs could
+          // be queued behind this very stage): V is released here, once both
+          // tiles are past the position.
           while (v_rel < npos && pp[0] > v_rel && pp[1] > v_rel) {
             tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
             ++v_rel;
@@ -460,8 +490,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int row0 = qb * 2 * C::BM + q * C::BM;
     const int row = row0 + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + q * C::BN;
-    const uint32_t tO = tmem + lane_off + 2 * C::BN + q * D;
+    const uint32_t tS = tmem + lane_off + C::TM_S + q * C::BN;
+    const uint32_t tO = tmem + lane_off + C::TM_O + q * D;
+    const uint32_t tP = tmem + lane_off + C::TM_P + q * C::TM_PSTRIDE;
     float m = -INFINITY;   // reference max (log2 units), moved lazily
     float l_exact = 0.f;   // sum of exp2(t - m) in fp32: gives LSE
     float l_round = 0.f;   // sum of the rounded P values: normalises O
@@ -488,9 +519,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
     };
     if (nk > 0) draw_tile(0);  // dropout is dense: tile j starts at key j * 128
+    // K/V stage release: stage p % NST of position p may be refilled once the
+    // MMAs of both tiles that read it have completed.  Each position's empty
+    // barrier takes two arrival units: one from each tile that uses it, or
+    // both from the only tile that does (thread 0 of the tile arrives).
+    //   K_p: S_q(p) is complete once this tile's S wait for p has returned;
+    //   V_p: P_q(p) V_p is complete once this tile has waited for it (SEPP:
+    //        the O wait of the next step; otherwise the next S wait, as S_q
+    //        is issued only after the previous P V has completed), or in the
+    //        epilogue for the tile's last position.  Dense only: a tile's
+    //        positions are consecutive there, so that next step never needs
+    //        a load queued behind the stage it holds (block-sparse, the
+    //        issuer releases V).
+    const int nkv_other = q ? nkv[0] : nkv[1];  // dense: positions the other tile uses
+    auto release = [&](int first_bar, int p) {
+      if (SPARSE && first_bar == C::B_VEMPTY) return;
+      const bool other = SPARSE ? ((pos_flags[p] >> (1 - q)) & 1) != 0 : p < nkv_other;
+      if (r == 0) mbar_arrive_cnt(bar(first_bar + p % C::NST), other ? 1u : 2u);
+    };
+    int prev_p = -1;  // position of this tile's previous step
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
       tc_fence_after_sync();
+      int pj = j;  // this step's position
+      if constexpr (SPARSE) {
+        while (!uses(q, pos)) ++pos;
+        pj = pos++;
+      }
+      release(C::B_KEMPTY, pj);
+      if (!C::SEPP && prev_p >= 0) release(C::B_VEMPTY, prev_p);
       float sv[128];
       {
         uint32_t u[64];
@@ -501,11 +558,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[64 + c] = __uint_as_float(u[c]);
       }
-      int kv0 = j * C::BN;
-      if constexpr (SPARSE) {
-        while (!uses(q, pos)) ++pos;
-        kv0 = kv_tile(pos++) * C::BN;
+      if constexpr (C::SEPP) {  // S_q may be overwritten by the next S now
+        tc_fence_before_sync();
+        mbar_arrive(bar(C::B_STAKEN + q));
       }
+      const int kv0 = kv_tile(pj) * C::BN;
       const bool masked = (kv0 + C::BN > N) || (causal && kv0 + C::BN - 1 > row0);
       int lim = C::BN;  // keys kv0 + c with c < lim are visible to this row
       if (masked) {
@@ -545,6 +602,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c >= lim) sv[c] = 0.f;
+      }
+      // With P apart (SEPP), P_q(j-1) V may still be running: its completion
+      // frees P_q and makes O_q final for the rescale below.  (At d = 128 it
+      // completed before S_q(j) was issued.)
+      if (C::SEPP && j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + q), (j - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after_sync();
+        release(C::B_VEMPTY, prev_p);
       }
       // O_q holds the previous steps' sum: rescale it when any row of this warp moved its max.
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -592,7 +658,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             }
           }
         }
-        tmem_st32(tS + c0 * 32, pk);
+        tmem_st32(tP + c0 * 32, pk);
         if (DROP && c0 == 0) {  // keys 0-63 of P (and any O correction) are in TMEM
           tmem_st_wait();
           tc_fence_before_sync();
@@ -605,6 +671,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL + q));
       if (DROP && j + 1 < nk) draw_tile((j + 1) * C::BN);
+      prev_p = pj;
     }
     // ------------------------------------------------------------ epilogue
     // At d = 128, O leaves through the tile's Q buffer in shared memory, which
@@ -619,6 +686,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     if constexpr (STAGE_O) ep = __all_sync(0xffffffffu, ep);
     if (ep) {
       tc_fence_after_sync();
+      release(C::B_VEMPTY, prev_p);
       const float inv_l = (DROP ? drop.rscale : 1.0f) / l_round;
       uint8_t* stage = smem + C::OFF_Q + q * C::TILE_BYTES;
       uint8_t* orow = o_out + (static_cast<int64_t>(bh) * N + row) * (D * 2);
