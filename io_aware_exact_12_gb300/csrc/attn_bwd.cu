@@ -96,8 +96,7 @@ struct BwdCfg {
   static constexpr int B_PFULL = B_DPFULL + 1;
   static constexpr int B_DVDONE = B_PFULL + 1;
   static constexpr int B_DSFULL = B_DVDONE + 1;
-  static constexpr int B_DSEMPTY = B_DSFULL + 1;
-  static constexpr int B_DQFULL = B_DSEMPTY + 1;
+  static constexpr int B_DQFULL = B_DSFULL + 1;
   static constexpr int B_DQEMPTY = B_DQFULL + 1;
   static constexpr int B_MMADONE = B_DQEMPTY + 1;
   static constexpr int NBAR = B_MMADONE + 1;
@@ -126,29 +125,28 @@ struct BwdCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// K-major descriptor, 16-element K slice kk, of a 128-row tile with head-dim rows.
+// Shared-memory descriptors as words (smem_desc_lo/hi): the issuer forms a
+// tile's low word once per MMA group and adds these offsets for the 16-deep K
+// slice kk.
+// K-major operand: a 128-row tile with head-dim rows (column chunks of one
+// swizzle width, CHUNK_BYTES apart).
 template <int D>
-__device__ __forceinline__ uint64_t desc_k_tile(uint32_t tile, int kk) {
+__host__ __device__ constexpr uint32_t k_tile_step(int kk) {
   using C = BwdCfg<D>;
-  const int e = kk * 16;
-  return smem_desc(tile + (e / C::CH) * C::CHUNK_BYTES + (e % C::CH) * 2, 16, C::SBO, C::SWZ);
+  return static_cast<uint32_t>(((kk * 16) / C::CH * C::CHUNK_BYTES + (kk * 16) % C::CH * 2) >> 4);
 }
-// MN-major descriptor (head dim contiguous), 16-row K slice kk.
+// MN-major operand: head dim contiguous, 16 rows per slice.
 template <int D>
-__device__ __forceinline__ uint64_t desc_mn_tile(uint32_t tile, int kk) {
-  using C = BwdCfg<D>;
-  return smem_desc(tile + kk * 16 * C::ROWB, C::CHUNK_BYTES, C::SBO, C::SWZ);
+__host__ __device__ constexpr uint32_t mn_tile_step(int kk) {
+  return static_cast<uint32_t>((kk * 16 * BwdCfg<D>::ROWB) >> 4);
 }
 // The dS^T tile: 128 key rows x 128 query columns, 128B-swizzled in two
 // 64-column chunks.  As dS^T (M = key, K = query) it is K-major ...
-__device__ __forceinline__ uint64_t desc_ds_kmajor(uint32_t tile, int kk) {
-  const int e = kk * 16;
-  return smem_desc(tile + (e / 64) * (128 * 128) + (e % 64) * 2, 16, 1024, kSwizzle128B);
+__host__ __device__ constexpr uint32_t ds_k_step(int kk) {
+  return static_cast<uint32_t>(((kk * 16) / 64 * (128 * 128) + (kk * 16) % 64 * 2) >> 4);
 }
-// ... and as dS (M = query, K = key) it is MN-major.
-__device__ __forceinline__ uint64_t desc_ds_mnmajor(uint32_t tile, int kk) {
-  return smem_desc(tile + kk * 16 * 128, 128 * 128, 1024, kSwizzle128B);
-}
+// ... and as dS (M = query, K = key) it is MN-major (LBO 128 * 128).
+__host__ __device__ constexpr uint32_t ds_mn_step(int kk) { return static_cast<uint32_t>((kk * 16 * 128) >> 4); }
 
 // Byte offset of 16-byte unit u of row `row` in the epilogue's staging copy of
 // a 128-row dK or dV tile (rows of 2 D = 256 bytes): the unit index is XOR-ed
@@ -361,7 +359,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_PFULL), 256);
     mbar_init(bar(C::B_DVDONE), 1);
     mbar_init(bar(C::B_DSFULL), 256);
-    mbar_init(bar(C::B_DSEMPTY), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQEMPTY), 128);
     mbar_init(bar(C::B_MMADONE), 1);
@@ -439,6 +436,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint32_t id_dv = instr_desc_f16(128, D, BF16, false, true);
       const uint32_t id_dk = instr_desc_f16(128, D, BF16, false, true);
       const uint32_t id_dq = instr_desc_f16(128, C::DQ_T ? 128 : D, BF16, true, true);
+      constexpr uint32_t HT = smem_desc_hi(C::SBO, C::SWZ);         // Q, K, V, dO tiles
+      constexpr uint32_t HDS = smem_desc_hi(1024, kSwizzle128B);    // the dS^T tile
+      const uint32_t k_klo = smem_desc_lo(sK, 16), v_klo = smem_desc_lo(sV, 16);
+      const uint32_t k_mnlo = smem_desc_lo(sK, C::CHUNK_BYTES);
+      const uint32_t ds_klo = smem_desc_lo(sDS, 16), ds_mnlo = smem_desc_lo(sDS, 128 * 128);
       bool ok = mbar_wait(bar(C::B_KVFULL), 0, abort_flag, status);
       tc_fence_after_sync();
       int is = 0, ip = 0, iv = 0, ik = 0;
@@ -449,11 +451,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (is < nq && is == iv && (is == 0 || mbar_probe(bar(C::B_DVDONE), (is - 1) & 1)) &&
             mbar_probe(bar(C::B_QFULL + is % C::NSTQ), (is / C::NSTQ) & 1)) {
           tc_fence_after_sync();
-          const uint32_t q_s = sQ + (is % C::NSTQ) * C::TILE_BYTES;
+          const uint32_t q_lo = smem_desc_lo(sQ + (is % C::NSTQ) * C::TILE_BYTES, 16);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::T_S, desc_k_tile<D>(sK, kk), desc_k_tile<D>(q_s, kk), id_st,
-                   kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + C::T_S, k_klo + k_tile_step<D>(kk), HT, q_lo + k_tile_step<D>(kk), HT, id_st,
+                     kk > 0 ? 1u : 0u);
           tc_commit(bar(C::B_SFULL));
           ++is;
           progress = true;
@@ -461,45 +463,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if (ip < nq && ip == ik && (ip == 0 || mbar_probe(bar(C::B_DQEMPTY), (ip - 1) & 1)) &&
             mbar_probe(bar(C::B_QFULL + ip % C::NSTQ), (ip / C::NSTQ) & 1)) {
           tc_fence_after_sync();
-          const uint32_t do_s = sDO + (ip % C::NSTQ) * C::TILE_BYTES;
+          const uint32_t do_lo = smem_desc_lo(sDO + (ip % C::NSTQ) * C::TILE_BYTES, 16);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + C::T_DP, desc_k_tile<D>(sV, kk), desc_k_tile<D>(do_s, kk), id_dpt,
-                   kk > 0 ? 1u : 0u);
+            mma_ss_w(tmem + C::T_DP, v_klo + k_tile_step<D>(kk), HT, do_lo + k_tile_step<D>(kk), HT, id_dpt,
+                     kk > 0 ? 1u : 0u);
           tc_commit(bar(C::B_DPFULL));
           ++ip;
           progress = true;
         }
         if (iv < is && mbar_probe(bar(C::B_PFULL), iv & 1)) {
           tc_fence_after_sync();
-          const uint32_t do_s = sDO + (iv % C::NSTQ) * C::TILE_BYTES;
+          const uint32_t do_lo = smem_desc_lo(sDO + (iv % C::NSTQ) * C::TILE_BYTES, C::CHUNK_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::BM / 16; ++kk)
-            mma_ts(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
-                   desc_mn_tile<D>(do_s, kk), id_dv, (iv > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_w(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                     do_lo + mn_tile_step<D>(kk), HT, id_dv, (iv > 0 || kk > 0) ? 1u : 0u);
           tc_commit(bar(C::B_DVDONE));
           ++iv;
           progress = true;
         }
         if (ik < iv && ik < ip && mbar_probe(bar(C::B_DSFULL), ik & 1)) {
           tc_fence_after_sync();
-          const uint32_t q_s = sQ + (ik % C::NSTQ) * C::TILE_BYTES;
+          const uint32_t q_mnlo = smem_desc_lo(sQ + (ik % C::NSTQ) * C::TILE_BYTES, C::CHUNK_BYTES);
 #pragma unroll
           for (int kk = 0; kk < C::BM / 16; ++kk)
-            mma_ss(tmem + C::T_DK, desc_ds_kmajor(sDS, kk), desc_mn_tile<D>(q_s, kk), id_dk,
-                   (ik > 0 || kk > 0) ? 1u : 0u);
+            mma_ss_w(tmem + C::T_DK, ds_klo + ds_k_step(kk), HDS, q_mnlo + mn_tile_step<D>(kk), HT, id_dk,
+                     (ik > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < C::BN / 16; ++kk) {
             if constexpr (C::DQ_T)  // dQ^T = K^T dS^T: both operands MN-major
-              mma_ss(tmem + C::T_DP, desc_mn_tile<D>(sK, kk), desc_ds_mnmajor(sDS, kk), id_dq,
-                     kk > 0 ? 1u : 0u);
+              mma_ss_w(tmem + C::T_DP, k_mnlo + mn_tile_step<D>(kk), HT, ds_mnlo + ds_mn_step(kk), HDS, id_dq,
+                       kk > 0 ? 1u : 0u);
             else                    // dQ = dS K
-              mma_ss(tmem + C::T_DP, desc_ds_mnmajor(sDS, kk), desc_mn_tile<D>(sK, kk), id_dq,
-                     kk > 0 ? 1u : 0u);
+              mma_ss_w(tmem + C::T_DP, ds_mnlo + ds_mn_step(kk), HDS, k_mnlo + mn_tile_step<D>(kk), HT, id_dq,
+                       kk > 0 ? 1u : 0u);
           }
+          // One commit tells three parties that dK(i) and dQ(i) (and every
+          // MMA before them) are complete: the dQ warps (dQ_i is in TMEM),
+          // the P/dS warps (the dS^T tile may be overwritten) and, through
+          // the P/dS warps' arrival, the producer (the Q_i, dO_i stage is
+          // free).  Two tcgen05.commit fewer per visit for the issuing thread.
           tc_commit(bar(C::B_DQFULL));
-          tc_commit(bar(C::B_QEMPTY + ik % C::NSTQ));
-          tc_commit(bar(C::B_DSEMPTY));
           ++ik;
           progress = true;
         }
@@ -596,12 +601,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
       if constexpr (DROP) {  // warp-uniform: the draws at the end of the visit shuffle
         ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status);
-        if (ok && it > 0) ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status);
+        if (ok && it > 0) ok = mbar_wait(bar(C::B_DQFULL), (it - 1) & 1, abort_flag, status);
+        // visit it-1's MMAs are all complete: its Q, dO stage may be refilled
+        if (ok && it > 0 && threadIdx.x == 0) mbar_arrive(bar(C::B_QEMPTY + (it - 1) % C::NSTQ));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       } else {
         if (!(ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status))) break;
-        if (it > 0 && !(ok = mbar_wait(bar(C::B_DSEMPTY), (it - 1) & 1, abort_flag, status))) break;
+        if (it > 0 && !(ok = mbar_wait(bar(C::B_DQFULL), (it - 1) & 1, abort_flag, status))) break;
+        // visit it-1's MMAs are all complete: its Q, dO stage may be refilled
+        if (it > 0 && threadIdx.x == 0) mbar_arrive(bar(C::B_QEMPTY + (it - 1) % C::NSTQ));
       }
       tc_fence_after_sync();
       const float2* nd = reinterpret_cast<const float2*>(sDD + s * C::BM + g * 64);  // -D
@@ -646,7 +655,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // then each warp stores its 32 rows with 512 contiguous bytes per
     // instruction (as the forward's O).  The warp takes the branch together.
     constexpr bool STAGE = (D == 128);
-    bool ep = ok && nq > 0 && mbar_wait(bar(C::B_DSEMPTY), (nq - 1) & 1, abort_flag, status);
+    bool ep = ok && nq > 0 && mbar_wait(bar(C::B_DQFULL), (nq - 1) & 1, abort_flag, status);
     if constexpr (STAGE) ep = __all_sync(0xffffffffu, ep);
     if (ep && half >= 0) {
       // a split item: this half's fp32 tile (x scale for dK, x 256/t for dV)

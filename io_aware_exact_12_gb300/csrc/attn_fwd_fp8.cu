@@ -21,8 +21,11 @@
 //   * l is kept twice (exact fp32 sum for LSE; sum of the e4m3-rounded P,
 //     converted back exactly through f16, to normalise O), and the epilogue
 //     multiplies by descale_v.
-// Roles, TMEM layout, ping-pong of two query tiles and the event-driven MMA
-// issuer are those of the bf16 kernel.
+// Roles, TMEM layout (S0 S1 O0 O1), ping-pong of two query tiles and the
+// event-driven MMA issuer are those of the bf16 kernel.  As P lives in shared
+// memory, S_q(j+1) goes out as soon as the softmax has read S_q(j) into
+// registers; the softmax waits for P_q(j) V_j only before it rescales O_q and
+// overwrites the P tile (as the bf16 kernel does at d <= 64).
 #include "attn_internal.h"
 #include "tc_sm103.cuh"
 
@@ -52,7 +55,8 @@ struct Fp8Cfg {
   static constexpr int B_PFULL = B_SFULL + 2;
   static constexpr int B_ODONE = B_PFULL + 2;
   static constexpr int B_MMADONE = B_ODONE + 2;
-  static constexpr int NBAR = B_MMADONE + 1;
+  static constexpr int B_STAKEN = B_MMADONE + 1;  // [2]: S_q read into registers
+  static constexpr int NBAR = B_STAKEN + 2;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 12;
@@ -65,23 +69,24 @@ struct Fp8Cfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-// K-major 8-bit operand tile: 128 rows x 128 bytes, 128-byte swizzle;
-// descriptor of the 32-element K slice kk.
-__device__ __forceinline__ uint64_t desc_k8(uint32_t tile, int kk) {
-  return smem_desc(tile + kk * 32, 16, 1024, kSwizzle128B);
-}
+// K-major 8-bit operand tiles: 128 rows x 128 bytes, 128-byte swizzle, 8-row
+// groups 1024 bytes apart; a 32-element K slice is 32 bytes along the row.
 
 // kind::f8f6f4 instruction descriptor: D = F32, A = B = E4M3 (format 0),
 // both K-major, M = 128, N = 128.
 constexpr uint32_t kIdescE4m3 = (1u << 4) | (0u << 7) | (0u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t accumulate) {
+// The same with the descriptors as words (smem_desc_lo/hi): the K slice kk of
+// a tile whose low word is lo starts at lo + 2 kk (32 bytes).
+constexpr uint32_t kHi8 = smem_desc_hi(1024, kSwizzle128B);
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                            uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(kIdescE4m3), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(kHi8), "r"(kIdescE4m3), "r"(accumulate)
       : "memory");
 }
 
@@ -173,14 +178,15 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 1);
+      mbar_init(bar(C::B_KEMPTY + s), 2);  // one unit per query tile (see the softmax)
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), 1);
+      mbar_init(bar(C::B_VEMPTY + s), 2);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar(C::B_SFULL + q), 1);
       mbar_init(bar(C::B_PFULL + q), C::BM);
       mbar_init(bar(C::B_ODONE + q), 1);
+      mbar_init(bar(C::B_STAKEN + q), C::BM);
     }
     mbar_init(bar(C::B_MMADONE), 1);
     *abort_flag = 0;
@@ -235,11 +241,14 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       }
     } else if (warp == 9 && lane == 0) {
       // -------------------------------------------------------- MMA issuer
-      // One S/PV chain per query tile, issued whenever ready (see attn_fwd.cu).
+      // One S/PV chain per query tile, issued whenever ready (see attn_fwd.cu):
+      //   S_q(j) needs K_j and the softmax done reading S_q(j-1);
+      //   PV_q(j) needs V_j^T and P_q(j) written to shared memory.
+      // The softmax threads release the K/V stages (see there).
       bool ok = nkv_max == 0 || mbar_wait(bar(C::B_QFULL), 0, abort_flag, status);
       tc_fence_after_sync();
+      const uint32_t q_lo0 = smem_desc_lo(sQ, 16), q_lo1 = smem_desc_lo(sQ + C::TILE_BYTES, 16);
       int js[2] = {0, 0}, jp[2] = {0, 0};
-      int k_rel = 0, v_rel = 0;
       IdleWatch watch;
       while (ok && (jp[0] < nkv[0] || jp[1] < nkv[1])) {
         bool progress = false;
@@ -251,38 +260,29 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
               mbar_probe(bar(C::B_VFULL + jv % C::NST), (jv / C::NST) & 1) &&
               mbar_probe(bar(C::B_PFULL + q), jv & 1)) {
             tc_fence_after_sync();
-            const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
-            const uint32_t p_s = sP + q * C::TILE_BYTES;
+            const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, 16);
+            const uint32_t p_lo = smem_desc_lo(sP + q * C::TILE_BYTES, 16);
 #pragma unroll
             for (int kk = 0; kk < C::BN / 32; ++kk)
-              mma_ss_f8(tmem + 2 * C::BN + q * D, desc_k8(p_s, kk), desc_k8(v_s, kk),
-                        (jv > 0 || kk > 0) ? 1u : 0u);
+              mma_ss_f8_w(tmem + 2 * C::BN + q * D, p_lo + 2 * kk, v_lo + 2 * kk, (jv > 0 || kk > 0) ? 1u : 0u);
             tc_commit(bar(C::B_ODONE + q));
             jp[q] = jv + 1;
             progress = true;
           }
           const int jk = js[q];
-          if (jk < nkv[q] && jk == jp[q] &&
+          if (jk < nkv[q] &&
               mbar_probe(bar(C::B_KFULL + jk % C::NST), (jk / C::NST) & 1) &&
-              (jk == 0 || mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1))) {
+              (jk == 0 || mbar_probe(bar(C::B_STAKEN + q), (jk - 1) & 1))) {
             tc_fence_after_sync();
-            const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
+            const uint32_t k_lo = smem_desc_lo(sK + (jk % C::NST) * C::TILE_BYTES, 16);
+            const uint32_t a_lo = q ? q_lo1 : q_lo0;
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk)
-              mma_ss_f8(tmem + q * C::BN, desc_k8(sQ + q * C::TILE_BYTES, kk), desc_k8(k_s, kk),
-                        kk > 0 ? 1u : 0u);
+              mma_ss_f8_w(tmem + q * C::BN, a_lo + 2 * kk, k_lo + 2 * kk, kk > 0 ? 1u : 0u);
             tc_commit(bar(C::B_SFULL + q));
             js[q] = jk + 1;
             progress = true;
           }
-        }
-        while (k_rel < nkv_max && (js[0] > k_rel || k_rel >= nkv[0]) && (js[1] > k_rel || k_rel >= nkv[1])) {
-          tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
-          ++k_rel;
-        }
-        while (v_rel < nkv_max && (jp[0] > v_rel || v_rel >= nkv[0]) && (jp[1] > v_rel || v_rel >= nkv[1])) {
-          tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
-          ++v_rel;
         }
         if (progress) {
           watch.progress();
@@ -308,11 +308,20 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     float m = -INFINITY;  // row max (log2 units) the weights are taken against, moved lazily
     float l_exact = 0.f, l_round = 0.f;
     bool ok = true;
-    const int nk = nkv[q];
+    const int nk = q ? nkv[1] : nkv[0];
+    const int nk_other = q ? nkv[0] : nkv[1];
     const float2 sl2x2 = make_float2(sl2, sl2);
+    // K/V stage release (as in attn_fwd.cu): each position's empty barrier
+    // takes one unit from each tile that uses it, or two from the only one.
+    // K_j is free once S_q(j) is complete (this tile's S wait); V_j once P_q(j)
+    // V_j is (the O wait of the next step, or the epilogue's).
+    auto release = [&](int first_bar, int p) {
+      if (r == 0) mbar_arrive_cnt(bar(first_bar + p % C::NST), p < nk_other ? 1u : 2u);
+    };
     for (int j = 0; j < nk; ++j) {
       if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
       tc_fence_after_sync();
+      release(C::B_KEMPTY, j);
       float sv[128];
       {
         uint32_t u[64];
@@ -323,6 +332,8 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) sv[64 + c] = __uint_as_float(u[c]);
       }
+      tc_fence_before_sync();
+      mbar_arrive(bar(C::B_STAKEN + q));  // S_q may be overwritten by the next S now
       const int kv0 = j * C::BN;
       const bool masked = (kv0 + C::BN > N) || (causal && kv0 + C::BN - 1 > row0);
       int lim = C::BN;
@@ -364,6 +375,14 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c >= lim) sv[c] = 0.f;
+      }
+      // P_q(j-1) V_{j-1} may still be running: it must finish before O_q is
+      // rescaled and before the P tile is overwritten.
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + q), (j - 1) & 1, abort_flag, status));
+        if (!ok) break;
+        tc_fence_after_sync();
+        release(C::B_VEMPTY, j - 1);
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -408,6 +427,7 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
     }
     if (ok && nk > 0 && mbar_wait(bar(C::B_ODONE + q), (nk - 1) & 1, abort_flag, status)) {
       tc_fence_after_sync();
+      release(C::B_VEMPTY, nk - 1);
       const float mul = descale_v / l_round;
       uint8_t* orow = o_out + (static_cast<int64_t>(bh) * N + row) * (D * 2);
 #pragma unroll
