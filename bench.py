@@ -432,13 +432,44 @@ def measure_dropout(attn, steps, warmup, peaks, p_drop=0.1):
     return res
 
 
+def bench_config(world):
+    """The `config` of both arms' lines (the same dict, so the two compare)."""
+    return dict(WORKLOAD, parallelism="dp%d (independent heads per rank)" % world)
+
+
+# Arm Ltd. (implementer 0x41) CPU part numbers of the cores these hosts carry;
+# /proc/cpuinfo on Arm gives only the number.
+ARM_PARTS = {0xd0c: "Neoverse-N1", 0xd40: "Neoverse-V1", 0xd49: "Neoverse-N2", 0xd4f: "Neoverse-V2",
+             0xd8e: "Neoverse-N3", 0xd84: "Neoverse-V3"}
+
+
 def cpu_model():
+    """A readable CPU model: lscpu's model name, else /proc/cpuinfo's, else the
+    Arm part number translated, with the part number beside it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                name = ln.split(":", 1)[1].strip()
+                if name and name != "-":
+                    return name
+    except (OSError, subprocess.SubprocessError):
+        pass
+    part = None
     try:
         for ln in open("/proc/cpuinfo"):
-            if ln.lower().startswith(("model name", "cpu part")):
+            key = ln.split(":", 1)[0].strip().lower()
+            if key == "model name":
                 return ln.split(":", 1)[1].strip()
+            if key == "cpu part" and part is None:
+                part = ln.split(":", 1)[1].strip()
     except OSError:
         pass
+    if part is not None:
+        try:
+            return "%s (CPU part %s)" % (ARM_PARTS[int(part, 16)], part)
+        except (KeyError, ValueError):
+            return "CPU part %s" % part
     import platform
     return platform.machine()
 
@@ -461,7 +492,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": dict(WORKLOAD),
+            "data": "synthetic", "config": bench_config(world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample, "cpu": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -694,7 +725,7 @@ def run_ours(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": dict(WORKLOAD, parallelism="dp%d (independent heads per rank)" % world),
+                "config": bench_config(world),
                 "fwd": {"ms": fwd_ms, "tflops": fwd_tf, "frac_of_peak": fwd_tf / peak},
                 "bwd": {"ms": bwd_ms, "tflops": bwd_tf, "frac_of_peak": bwd_tf / peak},
                 "causal": {"fwd_ms": statistics.median(cf_ms), "bwd_ms": statistics.median(cb_ms),

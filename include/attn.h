@@ -194,14 +194,18 @@ int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse
  * allocations once a fixed memory budget is set up, or hosts that give the
  * library only the tensors.  Parameters, layouts, ownership and results are
  * those of attn_bwd; the difference is where the scratch lives.  Instead of
- * the stream-ordered allocator it uses one fixed 32 MiB array in device
- * memory owned by the library (a GPU that loads the array keeps it until the
- * process exits).  The scratch a problem needs is
+ * the stream-ordered allocator it uses one fixed array of 34,078,720 bytes
+ * (32.5 MiB) in device memory owned by the library (a GPU that loads the
+ * array keeps it until the process exits).  The scratch a problem needs is
  *     align256(4*B*H*N*d) + 2 * align256(4*B*H*ceil(N/128)*128)   bytes;
- * a problem needing more than 32 MiB is rejected with ATTN_ERR_UNSUPPORTED
- * before anything is enqueued (use attn_bwd for it).
+ * B=1, H=8, N=8192, d=128 needs exactly the whole array.  A problem needing
+ * more is rejected with ATTN_ERR_UNSUPPORTED before anything is enqueued
+ * (use attn_bwd for it).
  *   - The first call on each device looks up the array's device address on
- *     that device; make that first call before any stream capture.
+ *     that device and caches it for the life of the process; make that first
+ *     call before any stream capture.  cudaDeviceReset discards the array
+ *     together with the context: do not call attn_bwd_noalloc on a device
+ *     after resetting it in the same process.
  *   - Every call on a device shares the one array.  A call rewrites all of
  *     the scratch it reads, so it does not depend on what an earlier call
  *     left there, but two calls that can run at the same time on the GPU
@@ -218,32 +222,6 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
  * ATTN_ERR_CUDA if the synchronisation itself failed.
  */
 int attn_sync_status(void* stream);
-
-/*
- * Self-test of the device failure path (the pages have no counterpart).
- * Enqueues one tiny kernel that runs the library's bounded pipeline wait on a
- * barrier nothing arrives on, with a limit of `limit_us` microseconds
- * (1 .. 2,000,000).  The wait gives up, the kernel records ATTN_ERR_TIMEOUT
- * in the sticky status and returns; a following attn_sync_status(stream)
- * returns ATTN_ERR_TIMEOUT and clears it.  Nothing hangs or faults; the
- * context stays usable.  Returns ATTN_OK if the kernel was enqueued.
- */
-int attn_debug_wait_timeout(int limit_us, void* stream);
-
-/*
- * Throughput probe of the exponential unit (a measurement aid; the pages have
- * no counterpart).  The softmax step needs one exp2 per score (B*H*N^2 per
- * forward, as many again in the backward's recomputation of P), so the
- * unit's rate bounds both passes next to the tensor cores.  Enqueues one
- * kernel of `blocks` x 256 threads; each thread runs `iters` rounds of 8
- * independent ex2.approx.f32 (the instruction the attention kernels use) and
- * writes one float to `sink`: caller-owned device memory of blocks * 256
- * floats, 4-byte aligned, overwritten.  Exponentials per launch =
- * blocks * 256 * iters * 8; time the launch with events on `stream`.
- * blocks 1 .. 65535, iters 1 .. 2^20, else ATTN_ERR_INVALID_ARG (nothing
- * enqueued).  Returns ATTN_OK once the kernel is enqueued.
- */
-int attn_probe_ex2(float* sink, int blocks, int iters, void* stream);
 
 /* Static, human-readable name of a status code (never NULL). */
 const char* attn_status_string(int status);

@@ -48,7 +48,7 @@ def _stale(target: str, deps) -> bool:
 
 def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "attn.h"), __file__]
+    headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, h) for h in ("attn.h", "attn_diag.h")] + [__file__]
     objs = []
     jobs = []
     for src in SOURCES:

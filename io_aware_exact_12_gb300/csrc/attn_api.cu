@@ -177,10 +177,7 @@ int device_sm_count() {
 }
 
 int bwd_tail_split(int BH, int N, int causal) {
-  if (causal) return 0;
-  const int64_t ntq = (static_cast<int64_t>(N) + 127) / 128;
-  if (ntq < 2) return 0;  // a key tile with one query tile has nothing to split
-  return tail_split_items(ntq * BH, device_sm_count());
+  return bwd_tail_split_items(BH, N, causal, device_sm_count());
 }
 
 int* status_word_current_device() {

@@ -1,4 +1,5 @@
-// attn_diag.cu -- diagnostics that sit beside the attention kernels.
+// attn_diag.cu -- diagnostics that sit beside the attention kernels (declared
+// in include/attn_diag.h, apart from the attention ABI of attn.h).
 //
 // 1. A self-test of the device-side failure path.  Every pipeline wait in the
 //    attention kernels is bounded; when one runs out the kernel records
@@ -13,6 +14,7 @@
 #include <cstdint>
 
 #include "attn.h"
+#include "attn_diag.h"
 #include "attn_internal.h"
 #include "tc_sm103.cuh"
 

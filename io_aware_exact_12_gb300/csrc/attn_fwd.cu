@@ -225,9 +225,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::NST; ++s) {
       mbar_init(bar(C::B_KFULL + s), 1);
-      mbar_init(bar(C::B_KEMPTY + s), 2);  // one unit per query tile (see the softmax)
+      // dense: one unit per query tile (the softmax releases); block-sparse:
+      // the issuer releases
+      mbar_init(bar(C::B_KEMPTY + s), SPARSE ? 1 : 2);
       mbar_init(bar(C::B_VFULL + s), 1);
-      mbar_init(bar(C::B_VEMPTY + s), SPARSE ? 1 : 2);  // block-sparse: the issuer releases V
+      mbar_init(bar(C::B_VEMPTY + s), SPARSE ? 1 : 2);
     }
     for (int q = 0; q < 2; ++q) {
       mbar_init(bar(C::B_SFULL + q), 1);
@@ -410,9 +412,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         int pp[2] = {0, 0};  // next position to consider for PV, per tile
         int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
         int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
-        int v_rel = 0;                 // next position whose V stage is still held
+        int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
         IdleWatch watch;
-        while (ok && (np[0] < cnt[0] || np[1] < cnt[1] || v_rel < npos)) {
+        while (ok && (k_rel < npos || v_rel < npos)) {
           bool progress = false;
           // Loads are observed strictly in position order: when position p is
           // probed, every earlier load on its stage has been seen, so the stage
@@ -432,11 +434,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               tc_fence_after_sync();
               const uint32_t d_o = tmem + C::TM_O + q * D;
               const uint32_t a_p = tmem + C::TM_P + q * C::TM_PSTRIDE;
-              const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, C::CHUNK_BYTES);
+              // (descriptor words at d <= 64; at d = 128 this issuer measured 9 %
+              // faster with the 64-bit descriptors formed per MMA)
+              if constexpr (C::SEPP) {
+                const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, C::CHUNK_BYTES);
   #pragma unroll
-              for (int kk = 0; kk < C::BN / 16; ++kk)
-                mma_ts_w(d_o, a_p + kk * 8, v_lo + mnmajor_lo_step<D>(kk), HI, idesc_o,
-                         (np[q] > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                  mma_ts_w(d_o, a_p + kk * 8, v_lo + mnmajor_lo_step<D>(kk), HI, idesc_o,
+                           (np[q] > 0 || kk > 0) ? 1u : 0u);
+              } else {
+                const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
+  #pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                  mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (np[q] > 0 || kk > 0) ? 1u : 0u);
+              }
               tc_commit(bar(C::B_ODONE + q));
               pp[q] = jv + 1;
               ++np[q];
@@ -449,23 +460,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
                                         : mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1)))) {
               tc_fence_after_sync();
               const uint32_t d_s = tmem + C::TM_S + q * C::BN;
-              const uint32_t a_lo = q ? q_lo1 : q_lo0;
-              const uint32_t k_lo = smem_desc_lo(sK + (jk % C::NST) * C::TILE_BYTES, 16);
+              if constexpr (C::SEPP) {
+                const uint32_t a_lo = q ? q_lo1 : q_lo0;
+                const uint32_t k_lo = smem_desc_lo(sK + (jk % C::NST) * C::TILE_BYTES, 16);
   #pragma unroll
-              for (int kk = 0; kk < D / 16; ++kk)
-                mma_ss_w(d_s, a_lo + kmajor_lo_step<D>(kk), HI, k_lo + kmajor_lo_step<D>(kk), HI, idesc_s,
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_ss_w(d_s, a_lo + kmajor_lo_step<D>(kk), HI, k_lo + kmajor_lo_step<D>(kk), HI, idesc_s,
+                           kk > 0 ? 1u : 0u);
+              } else {
+                const uint32_t k_s = sK + (jk % C::NST) * C::TILE_BYTES;
+  #pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                  mma_ss(d_s, desc_kmajor<D>(sQ + q * C::TILE_BYTES, kk), desc_kmajor<D>(k_s, kk), idesc_s,
                          kk > 0 ? 1u : 0u);
+              }
               tc_commit(bar(C::B_SFULL + q));
               sp[q] = jk + 1;
               ++ns[q];
               progress = true;
             }
           }
-          // A tile holds a position's V until its P V completes; under a block
-          // mask its next position may lie beyond the ring, so the softmax
-          // cannot release V from its next step's wait (the load it needs could
-          // be queued behind this very stage): V is released here, once both
-          // tiles are past the position.
+          // Under a block mask the stages are released here, once both tiles
+          // are past a position: a tile's next position may lie beyond the
+          // ring, so the softmax could not release V from its next step's wait
+          // (the load it needs could be queued behind this very stage); K is
+          // released here too, which keeps this loop as it measured fastest.
+          while (k_rel < npos && sp[0] > k_rel && sp[1] > k_rel) {
+            tc_commit(bar(C::B_KEMPTY + k_rel % C::NST));
+            ++k_rel;
+          }
           while (v_rel < npos && pp[0] > v_rel && pp[1] > v_rel) {
             tc_commit(bar(C::B_VEMPTY + v_rel % C::NST));
             ++v_rel;
@@ -527,15 +550,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     //   V_p: P_q(p) V_p is complete once this tile has waited for it (SEPP:
     //        the O wait of the next step; otherwise the next S wait, as S_q
     //        is issued only after the previous P V has completed), or in the
-    //        epilogue for the tile's last position.  Dense only: a tile's
-    //        positions are consecutive there, so that next step never needs
-    //        a load queued behind the stage it holds (block-sparse, the
-    //        issuer releases V).
+    //        epilogue for the tile's last position.
+    // Dense only: a tile's positions are consecutive there, so that next step
+    // never needs a load queued behind the stage it holds (block-sparse, the
+    // issuer releases both).
     const int nkv_other = q ? nkv[0] : nkv[1];  // dense: positions the other tile uses
     auto release = [&](int first_bar, int p) {
-      if (SPARSE && first_bar == C::B_VEMPTY) return;
-      const bool other = SPARSE ? ((pos_flags[p] >> (1 - q)) & 1) != 0 : p < nkv_other;
-      if (r == 0) mbar_arrive_cnt(bar(first_bar + p % C::NST), other ? 1u : 2u);
+      if (SPARSE) return;
+      if (r == 0) mbar_arrive_cnt(bar(first_bar + p % C::NST), p < nkv_other ? 1u : 2u);
     };
     int prev_p = -1;  // position of this tile's previous step
     for (int j = 0; j < nk; ++j) {

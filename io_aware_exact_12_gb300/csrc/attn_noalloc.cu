@@ -13,7 +13,9 @@
 // GPU that loads it keeps it until the process exits (with the CUDA runtime's
 // default lazy module loading that happens at the latest on the first call on
 // that device).  Its device address is looked up once per device, by the
-// first call made with that device current.
+// first call made with that device current, and cached for the life of the
+// process; a cudaDeviceReset of that device discards the array with the
+// context, so the cached address must not be used after one.
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -21,9 +23,10 @@
 #include "attn.h"
 #include "attn_internal.h"
 
-// 32 MiB: enough for B*H*N*d up to about 8 million elements (e.g. B=1, H=8,
-// N=8192, d=128).  The exact rule is in attn.h.
-constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+// 32.5 MiB: the dQ accumulator of 8 Mi elements of B*H*N*d (32 MiB) plus the
+// two per-row vectors of such a problem (2 x 256 KiB at N = 8192), so that,
+// for example, B=1, H=8, N=8192, d=128 fits exactly.  The rule is in attn.h.
+constexpr size_t kNoAllocScratchBytes = (size_t(32) << 20) + (size_t(512) << 10);
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

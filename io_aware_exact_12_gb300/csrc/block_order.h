@@ -52,6 +52,16 @@ __host__ __device__ inline int tail_split_items(int64_t W, int S) {
   return (r > 0 && 2 * r <= S) ? static_cast<int>(r) : 0;
 }
 
+// The backward's use of it: without the causal mask every (key tile, head)
+// item costs the same, so the ceil(N/128) * BH items on `sms` SMs may end with
+// a short wave; a key tile with a single query tile has nothing to split.
+__host__ __device__ inline int bwd_tail_split_items(int BH, int N, int causal, int sms) {
+  if (causal) return 0;
+  const int64_t ntq = (static_cast<int64_t>(N) + 127) / 128;
+  if (ntq < 2) return 0;
+  return tail_split_items(ntq * BH, sms);
+}
+
 // Block b of a grid of W + r blocks whose last r items are split (split_from =
 // W - r): the item it works on, which half of the item's range (-1: all) and,
 // for a split item, its pair index item - split_from.  Blocks below

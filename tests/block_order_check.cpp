@@ -3,7 +3,8 @@
 //    every grid of nblk x BH blocks and every head-group size, the linear block
 //    indices map one-to-one onto (rank, head) pairs, ranks run heaviest-first
 //    within a group, and a group holds at most g heads;
-//  - tail_split_items / split_block_item (the backward's split last wave):
+//  - tail_split_items / split_block_item / bwd_tail_split_items (the
+//    backward's split last wave):
 //    the split items are exactly the last partial wave when it is at most half
 //    the SMs, and the grid's blocks cover every unsplit item once and both
 //    halves of every split item.
@@ -95,6 +96,21 @@ int main() {
         }
       }
       ++cases;
+    }
+  }
+  // the backward's policy: never under the causal mask or for a single query
+  // tile; otherwise the generic rule over ceil(N / 128) * BH items
+  for (int S : {148, 152}) {
+    for (int BH = 1; BH <= 40; BH += 3) {
+      for (int N : {1, 128, 129, 1000, 8192, 32768}) {
+        const int ntq = (N + 127) / 128;
+        const int want = ntq < 2 ? 0 : attn::tail_split_items(static_cast<int64_t>(ntq) * BH, S);
+        if (attn::bwd_tail_split_items(BH, N, 1, S) != 0 || attn::bwd_tail_split_items(BH, N, 0, S) != want) {
+          std::printf("bwd tail split: BH=%d N=%d S=%d\n", BH, N, S);
+          return 1;
+        }
+        ++cases;
+      }
     }
   }
   std::printf("%d grids ok\n", cases);

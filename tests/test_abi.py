@@ -1,6 +1,7 @@
 """C-ABI checks that need no GPU: the library builds and loads, exports every
-function include/attn.h declares, and rejects bad arguments synchronously
-(before any CUDA call, so nothing is launched)."""
+function the headers under include/ declare (the attention ABI attn.h and the
+diagnostics attn_diag.h), and rejects bad arguments synchronously (before
+any CUDA call, so nothing is launched)."""
 import ctypes
 import os
 import re
@@ -10,7 +11,8 @@ import pytest
 from io_aware_exact_12_gb300 import build as build_mod
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "attn.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 
 @pytest.fixture(scope="module")
@@ -20,18 +22,24 @@ def L():
     return pkg.lib()
 
 
-def declared_functions():
-    text = open(HEADER, encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(attn_\w+)\s*\(", text, flags=re.M)
-    return sorted(set(names))
+def declared_functions(headers=None):
+    names = set()
+    for h in headers or HEADERS:
+        text = open(h, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(attn_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_boundary():
-    names = declared_functions()
+    names = declared_functions([os.path.join(ROOT, "include", "attn.h")])
     for required in ("attn_fwd", "attn_bwd", "attn_fwd_f16", "attn_bwd_f16", "attn_sync_status",
                      "attn_status_string"):
         assert required in names
+    # the measurement aid and the failure-path self-test are not attention
+    assert "attn_probe_ex2" not in names and "attn_debug_wait_timeout" not in names
+    diag = declared_functions([os.path.join(ROOT, "include", "attn_diag.h")])
+    assert diag == ["attn_debug_wait_timeout", "attn_probe_ex2"]
 
 
 def test_library_exports_every_declared_symbol(L):

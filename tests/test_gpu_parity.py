@@ -189,17 +189,19 @@ def test_c4_long_sequence(causal):
     s = 1.0 / math.sqrt(128)
     o, lse = gpu_fwd(x, s, causal)
     grads = gpu_bwd(x, o, lse, s, causal)
-    _check_sampled(x, s, causal, o, lse, grads, nrows=512, heads_for_cols=[0, 31], ncols=64)
+    _check_sampled(x, s, causal, o, lse, grads, nrows=512, heads_for_cols=[0, 11, 20, 31], ncols=64)
     _check_identities(x, grads)
 
 
-# 5: very long single sequence, B=1 H=8 N=32768 d=128 bf16 causal; 512 sampled query rows
+# 5: very long single sequence, B=1 H=8 N=32768 d=128 bf16 causal; 512 sampled
+# query rows (O, LSE, dQ) and 512 sampled key columns, 64 in each of the 8
+# heads (dK, dV; the oracle streams every row's LSE and D of each head)
 def test_c5_very_long_sequence():
     x = make_inputs(AttnShape(1, 8, 32768, 128), "bf16", seed=5)
     s = 1.0 / math.sqrt(128)
     o, lse = gpu_fwd(x, s, True)
     grads = gpu_bwd(x, o, lse, s, True)
-    _check_sampled(x, s, True, o, lse, grads, nrows=512, heads_for_cols=[7], ncols=32)
+    _check_sampled(x, s, True, o, lse, grads, nrows=512, heads_for_cols=list(range(8)), ncols=64)
     _check_identities(x, grads)
 
 
@@ -282,11 +284,28 @@ def test_worked_example_on_gpu(scale):
     assert abs(lse[0, 0, 0].item() - (scale * 95.0 + math.log(ell))) <= TOL_LSE
 
 
-def test_constant_v_and_uniform_rows():
-    x = make_inputs(AttnShape(2, 2, 300, 64), "bf16", seed=8)
-    x["v"] = torch.ones_like(x["v"])
-    o, _ = gpu_fwd(x, 0.125, True)
-    assert (o.float() - 1.0).abs().max().item() <= TOL_O
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v(d, causal):
+    """Every row of V equal to one vector c (per head): the weights of a row sum
+    to 1, so O_i = c exactly for every row; and dP_ij = dO_i . c = D_i for every
+    key, so dS = 0 and dQ = dK = 0 exactly (only rounding remains), while
+    dV = P^T dO is unchanged in form."""
+    B, H, N = 2, 2, 300
+    x = make_inputs(AttnShape(B, H, N, d), "bf16", seed=8 + d)
+    c = torch.randn(B, H, 1, d, generator=torch.Generator().manual_seed(d)).bfloat16()
+    s = 1.0 / math.sqrt(d)
+    grads_random_v = gpu_bwd(x, *gpu_fwd(x, s, causal), s, causal)
+    x["v"] = c.expand(B, H, N, d).contiguous()
+    o, lse = gpu_fwd(x, s, causal)
+    check_o(o, np.broadcast_to(f64(c), (B, H, N, d)))
+    oo, _ = check_fwd_full(x, s, causal, o, lse)
+    dq, dk, dv = gpu_bwd(x, o, lse, s, causal)
+    for name, g, ref in (("dq", dq, grads_random_v[0]), ("dk", dk, grads_random_v[1])):
+        ratio = float(g.float().norm() / ref.float().norm())
+        assert ratio <= TOL_GRAD, "%s is %g of its size with a random V" % (name, ratio)
+    _, _, dv_ref = oracle.backward(f64(x["q"]), f64(x["k"]), f64(x["v"]), oo, f64(x["do"]), s, causal)
+    assert rel_fro(f64(dv), dv_ref) <= TOL_GRAD
 
 
 # ----------------------------------------------------- causal bit-exactness
@@ -319,14 +338,28 @@ def test_forward_is_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_key_shift_invariance_on_gpu():
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance_on_gpu(causal):
+    """Adding one vector c to every key adds scale * q_i . c to every score of
+    row i, which the softmax removes: O is unchanged and LSE_i moves by
+    scale * q_i . c.  K is put on a grid of 1/16 in [-4, 4) so that K + 1/2 is
+    exact in bf16 (at most 7 significant bits); both runs are compared with
+    each other and with the oracle of the unshifted problem."""
     x = make_inputs(AttnShape(1, 2, 256, 64), "bf16", seed=12)
-    o1, _ = gpu_fwd(x, 0.125, False)
+    x["k"] = ((x["k"].float() * 16).round().clamp(-64, 63) / 16).bfloat16()
+    shifted = x["k"].float() + 0.5
+    assert torch.equal(shifted.bfloat16().float(), shifted)  # the shift is exact
     y = dict(x)
-    y["k"] = (x["k"].float() + 0.5).bfloat16()  # a shift every key shares (exact in bf16 here? not needed)
-    o2, _ = gpu_fwd(y, 0.125, False)
-    oo, _ = oracle.forward(f64(y["q"]), f64(y["k"]), f64(y["v"]), 0.125, False)
-    assert np.abs(f64(o2) - oo).max() <= TOL_O
+    y["k"] = shifted.bfloat16()
+    o1, l1 = gpu_fwd(x, 0.125, causal)
+    o2, l2 = gpu_fwd(y, 0.125, causal)
+    oo, lo = oracle.forward(f64(x["q"]), f64(x["k"]), f64(x["v"]), 0.125, causal)
+    check_o(o1, oo)
+    check_o(o2, oo)  # the shifted problem has the same exact O
+    assert (o1.float() - o2.float()).abs().max().item() <= 2 * TOL_O
+    lse_shift = 0.125 * 0.5 * f64(x["q"]).sum(-1)
+    assert np.abs(f64(l2) - f64(l1) - lse_shift).max() <= 2 * TOL_LSE
+    assert np.abs(f64(l2) - (lo + lse_shift)).max() <= TOL_LSE
 
 
 def test_launch_count_and_status():
