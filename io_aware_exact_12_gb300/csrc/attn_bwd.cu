@@ -42,7 +42,10 @@
 //                  At d = 128 the MMA produces dQ_i^T = K_j^T dS^T instead, so a
 //                  thread holds one head-dim column and each warp-wide reduction
 //                  is 128 contiguous bytes of a dQ row (8x fewer L2 requests
-//                  than row-per-thread 16-byte vector reductions).
+//                  than row-per-thread 16-byte vector reductions); at d <= 64
+//                  (dQ_i = dS K_j, a thread per query row) groups of 8 lanes
+//                  transpose their 16-byte pieces so that each 16-byte vector
+//                  reduction instruction covers 4 whole 128-byte row segments.
 //   * warps 14-15: idle (they complete warpgroup 3 for the register split).
 //   * TMEM (512 columns): S^T/P^T [0,128) dP^T/dQ [128,256) dK [256,256+D)
 //                         dV [256+D,256+2D).
@@ -730,8 +733,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     int qi = i0 - 1;
     for (int it = 0; it < nq; ++it) {
       const int q0 = ATTN_BWD_QTILE(it, qi) * C::BM;
-      const int qrow = q0 + t;
-      if (!mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status)) break;
+      // warp-uniform (the d <= 64 reductions below shuffle across the warp)
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status))) break;
       tc_fence_after_sync();
       uint32_t v[NCOL];
 #pragma unroll
@@ -751,12 +754,50 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < C::BM; ++c)
           if (c < nrow) red_add_f32(dst + static_cast<int64_t>(c) * D, __uint_as_float(v[c]) * scale);
-      } else if (qrow < N) {
-        float* dst = dq_acc + (static_cast<int64_t>(bh) * N + qrow) * D;
+      } else {
+        // Thread t holds query row q0 + t (d <= 64: 64 or 32 floats).  Each group
+        // of 8 lanes (rows r0..r7) transposes its 16-byte pieces in blocks of
+        // 8 x 8 (three shuffle stages, each swapping one bit of the lane index
+        // with the same bit of the piece index), so that reduction k of a
+        // block writes row r_k's 8 pieces, 128 contiguous bytes, from the 8
+        // lanes: each warp instruction covers 4 whole lines instead of 32
+        // scattered half-sectors.  Measured at B=2 H=16 N=8192 d=64: 540
+        // TFLOP/s with the scattered form, 642 with lane pairs covering
+        // 32-byte sectors, 665 with these 128-byte rows: the L2's reduction
+        // throughput is counted in sectors.
+        const int l8 = t & 7;
+        const int row0 = q0 + (t & ~7);
 #pragma unroll
-        for (int c = 0; c < D; c += 4)
-          red_add_v4(dst + c, __uint_as_float(v[c]) * scale, __uint_as_float(v[c + 1]) * scale,
-                     __uint_as_float(v[c + 2]) * scale, __uint_as_float(v[c + 3]) * scale);
+        for (int g = 0; g < D / 32; ++g) {  // groups of 8 pieces (32 floats)
+          float w[8][4];
+#pragma unroll
+          for (int p = 0; p < 8; ++p)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[p][e] = __uint_as_float(v[32 * g + 4 * p + e]);
+          // stage b: lanes differing in bit b exchange pieces whose index bit b differs from their lane bit b
+#pragma unroll
+          for (int b = 0; b < 3; ++b) {
+            const int m = 1 << b;
+            const bool hi = (l8 & m) != 0;
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+              if (p & m) continue;  // handle pairs (p, p | m)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                // lane with bit clear keeps piece p, sends p|m; lane with bit set keeps p|m, sends p
+                const float send = hi ? w[p][e] : w[p | m][e];
+                const float got = __shfl_xor_sync(0xffffffffu, send, m);
+                if (hi) w[p][e] = got; else w[p | m][e] = got;
+              }
+            }
+          }
+          // now lane l8 holds piece l8 of rows row0 + k in w[k]
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (row0 + k < N)
+              red_add_v4(dq_acc + (static_cast<int64_t>(bh) * N + row0 + k) * D + 32 * g + 4 * l8,
+                         w[k][0] * scale, w[k][1] * scale, w[k][2] * scale, w[k][3] * scale);
+        }
       }
     }
   }
