@@ -97,8 +97,7 @@ struct BwdCfg {
   static constexpr int B_SFULL = B_QEMPTY + NSTQ;
   static constexpr int B_DPFULL = B_SFULL + 1;
   static constexpr int B_PFULL = B_DPFULL + 1;
-  static constexpr int B_DVDONE = B_PFULL + 1;
-  static constexpr int B_DSFULL = B_DVDONE + 1;
+  static constexpr int B_DSFULL = B_PFULL + 1;
   static constexpr int B_DQFULL = B_DSFULL + 1;
   static constexpr int B_DQEMPTY = B_DQFULL + 1;
   static constexpr int B_MMADONE = B_DQEMPTY + 1;
@@ -360,7 +359,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PFULL), 256);
-    mbar_init(bar(C::B_DVDONE), 1);
     mbar_init(bar(C::B_DSFULL), 256);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQEMPTY), 128);
@@ -430,10 +428,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // Four chains over the query tiles i, each group issued as soon as ready
       // (checked in pipeline order: S, dP, dV, then dK/dQ, which measured 0.5-3 %
       // faster than the reverse order):
-      //   S(i)  = K Q_i^T   needs Q_i resident and dV(i-1) complete (P^T aliases S^T)
+      //   S(i)  = K Q_i^T   needs Q_i resident and dV(i-1) issued (P^T aliases S^T;
+      //                     see below)
       //   dP(i) = V dO_i^T  needs dO_i resident and dQ(i-1) read out (dQ aliases dP^T)
       //   dV(i)             needs P^T(i) in TMEM
       //   dK(i), dQ(i)      need dS^T(i) in shared memory (and dV(i) issued)
+      // S(i) overwrites the P^T(i-1) that dV(i-1) reads from TMEM.  It is issued
+      // right after dV(i-1), without waiting for dV(i-1) to complete: the tensor
+      // pipe executes one thread's MMAs in issue order, so dV(i-1) has read its
+      // A operand before S(i) writes.  (The PTX ISA promises this order only
+      // for MMAs into the same accumulator; on GB300 the in-order form gave
+      // bit-identical dK and dV in every repeated run of every configuration
+      // tried, and saves the issuer a commit and the S chain a completion
+      // round trip per visit.)
       const uint32_t id_st = instr_desc_f16(128, 128, BF16, false, false, negate != 0);
       const uint32_t id_dpt = instr_desc_f16(128, 128, BF16, false, false);
       const uint32_t id_dv = instr_desc_f16(128, D, BF16, false, true);
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       while (ok && ik < nq) {
         bool progress = false;
         // (the barrier that usually decides is probed first: Q_i, dO_i have long landed)
-        if (is < nq && is == iv && (is == 0 || mbar_probe(bar(C::B_DVDONE), (is - 1) & 1)) &&
+        if (is < nq && is == iv &&
             mbar_probe(bar(C::B_QFULL + is % C::NSTQ), (is / C::NSTQ) & 1)) {
           tc_fence_after_sync();
           const uint32_t q_lo = smem_desc_lo(sQ + (is % C::NSTQ) * C::TILE_BYTES, 16);
@@ -482,7 +489,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           for (int kk = 0; kk < C::BM / 16; ++kk)
             mma_ts_w(tmem + C::T_DV, tmem + C::T_S + (kk >> 2) * 64 + (kk & 3) * 8,
                      do_lo + mn_tile_step<D>(kk), HT, id_dv, (iv > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(bar(C::B_DVDONE));
           ++iv;
           progress = true;
         }

@@ -31,8 +31,9 @@
 //               values (the weights actually applied to V) to normalise O.
 //   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
 //     at d <= 64 also P0, P1 (64 columns each) after O1, so a tile's next S
-//     goes out once its softmax has read the current S instead of after the
-//     current P V has finished; at d = 128 P_q overwrites half of S_q.
+//     goes out once its softmax has read the current S; at d = 128 P_q
+//     overwrites half of S_q, and the tile's next S goes out right after the
+//     current P V (the tensor pipe runs one thread's MMAs in issue order).
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied; only the diagonal tile (and the ragged last tile) are masked;
 // the CTAs run heaviest first across a group of heads (block_order.h).
@@ -97,7 +98,8 @@ struct FwdCfg {
   // At d <= 64, P_q has TMEM columns of its own after O0, O1 (64 columns of
   // packed 16-bit values each), so S_q(j+1) can be computed as soon as the
   // softmax has read S_q(j), while P_q(j) V_j is still pending.  At d = 128
-  // the 512 columns are full and P_q overwrites the first half of S_q.
+  // the 512 columns are full and P_q overwrites the first half of S_q, so
+  // S_q(j+1) follows P_q(j) V_j in the tensor pipe's issue order.
   static constexpr bool SEPP = (D <= 64);
   static constexpr uint32_t TM_S = 0;                            // + 128 q
   static constexpr uint32_t TM_O = 2 * BN;                       // + D q
@@ -311,8 +313,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       // Each query tile runs its own chain S, PV, S, PV, ... over the positions
       // it uses; the issuer polls both chains and issues whichever next MMA
       // group is ready, so one tile's softmax never holds up the other's MMAs.
-      //   S_q at position p  needs K_p resident and the tile's previous PV
-      //                      complete (P_q aliases S_q);
+      //   S_q at position p  needs K_p resident and, with P in S's columns
+      //                      (d = 128), the tile's previous PV issued;
       //   PV_q at position p needs V_p resident and P_q written by the softmax.
       // The K and V stages are released by the softmax threads (below), which
       // learn from their own waits when the MMAs reading a stage have
@@ -376,14 +378,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               half[q] = false;
               progress = true;
             }
-            // S_q(js).  With P in S's columns (d = 128) it needs the tile's
-            // previous P V complete; with P apart (SEPP) only the previous S
-            // read out by the softmax.
+            // S_q(js).  With P apart (SEPP) it needs the previous S read out
+            // by the softmax.  With P in S's columns (d = 128) it needs the
+            // tile's previous P V issued, not complete: S_q(j+1) overwrites the
+            // P_q(j) that P_q(j) V reads from TMEM, and the tensor pipe executes
+            // one thread's MMAs in issue order, so that read happens first.
+            // (The PTX ISA promises this order only for MMAs into the same
+            // accumulator; on GB300 the in-order form gave bit-identical
+            // results in every repeated run of every configuration tried, and
+            // saves the chain a completion round trip per step: +4 % at d = 128.)
+            // The softmax's own waits are unaffected: the commit that signals
+            // S_q(j+1) tracks every MMA issued before it, P_q(j) V included.
             const int jk = js[q];
             if (jk < nkv[q] && (C::SEPP || jk == jp[q]) &&
                 mbar_probe(bar(C::B_KFULL + jk % C::NST), (jk / C::NST) & 1) &&
-                (jk == 0 || (C::SEPP ? mbar_probe(bar(C::B_STAKEN + q), (jk - 1) & 1)
-                                     : mbar_probe(bar(C::B_ODONE + q), (jk - 1) & 1)))) {
+                (jk == 0 || !C::SEPP || mbar_probe(bar(C::B_STAKEN + q), (jk - 1) & 1))) {
               tc_fence_after_sync();
               const uint32_t d_s = tmem + C::TM_S + q * C::BN;
               const uint32_t a_lo = q ? q_lo1 : q_lo0;
@@ -456,8 +465,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             // S_q at sp
             const int jk = sp[q];
             if (jk < npos && (C::SEPP || ns[q] == np[q]) && jk < k_ready &&
-                (ns[q] == 0 || (C::SEPP ? mbar_probe(bar(C::B_STAKEN + q), (ns[q] - 1) & 1)
-                                        : mbar_probe(bar(C::B_ODONE + q), (np[q] - 1) & 1)))) {
+                (ns[q] == 0 || !C::SEPP || mbar_probe(bar(C::B_STAKEN + q), (ns[q] - 1) & 1))) {
               tc_fence_after_sync();
               const uint32_t d_s = tmem + C::TM_S + q * C::BN;
               if constexpr (C::SEPP) {
@@ -548,9 +556,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // both from the only tile that does (thread 0 of the tile arrives).
     //   K_p: S_q(p) is complete once this tile's S wait for p has returned;
     //   V_p: P_q(p) V_p is complete once this tile has waited for it (SEPP:
-    //        the O wait of the next step; otherwise the next S wait, as S_q
-    //        is issued only after the previous P V has completed), or in the
-    //        epilogue for the tile's last position.
+    //        the O wait of the next step; otherwise the next S wait, whose
+    //        commit tracks every MMA issued before that S, P V included), or
+    //        in the epilogue for the tile's last position.
     // Dense only: a tile's positions are consecutive there, so that next step
     // never needs a load queued behind the stage it holds (block-sparse, the
     // issuer releases both).
@@ -627,7 +635,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       // With P apart (SEPP), P_q(j-1) V may still be running: its completion
       // frees P_q and makes O_q final for the rescale below.  (At d = 128 it
-      // completed before S_q(j) was issued.)
+      // was issued before S_q(j), so the S wait above covers it.)
       if (C::SEPP && j > 0) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_ODONE + q), (j - 1) & 1, abort_flag, status));
         if (!ok) break;
