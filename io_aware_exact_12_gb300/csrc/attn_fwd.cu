@@ -668,6 +668,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
       // P is rounded to the input type for the P V product.
+      if constexpr (!DROP && !C::SEPP) {
+        // d = 128 without dropout: P goes out first and the two row sums
+        // follow, overlapping the P V product instead of delaying it (+2 %;
+        // at d = 32 the same order measured 7 % slower, at d = 64 no change).
+        uint32_t pk0[32], pk1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk0[i] = pack2<BF16>(sv[2 * i], sv[2 * i + 1]);
+        tmem_st32(tP, pk0);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk1[i] = pack2<BF16>(sv[64 + 2 * i], sv[64 + 2 * i + 1]);
+        tmem_st32(tP + 32, pk1);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(bar(C::B_PFULL + q));
+        float2 se0 = make_float2(0.f, 0.f), se1 = se0;
+        float sr0 = 0.f, sr1 = 0.f, sr2 = 0.f, sr3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          se0 = add2(se0, make_float2(sv[c], sv[c + 1]));
+          se1 = add2(se1, make_float2(sv[c + 2], sv[c + 3]));
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          sr0 = add_halves<BF16>(sr0, pk0[i]);
+          sr1 = add_halves<BF16>(sr1, pk0[i + 1]);
+          sr2 = add_halves<BF16>(sr2, pk1[i]);
+          sr3 = add_halves<BF16>(sr3, pk1[i + 1]);
+        }
+        l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
+        l_round = l_round * alpha + ((sr0 + sr1) + (sr2 + sr3));
+        prev_p = pj;
+        continue;
+      }
       float2 se0 = make_float2(0.f, 0.f), se1 = se0;
       float sr0 = 0.f, sr1 = 0.f, sr2 = 0.f, sr3 = 0.f;
 #pragma unroll
