@@ -583,7 +583,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     };
     int prev_p = -1;  // position of this tile's previous step
     for (int j = 0; j < nk; ++j) {
-      if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
+      // warp-uniform, as the step votes across the warp (rescale) further on:
+      // a lane that left alone would leave the others waiting at the vote
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status)))) break;
       tc_fence_after_sync();
       int pj = j;  // this step's position
       if constexpr (SPARSE) {

@@ -319,7 +319,9 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
       if (r == 0) mbar_arrive_cnt(bar(first_bar + p % C::NST), p < nk_other ? 1u : 2u);
     };
     for (int j = 0; j < nk; ++j) {
-      if (!(ok = mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status))) break;
+      // warp-uniform, as the step votes across the warp (rescale) further on:
+      // a lane that left alone would leave the others waiting at the vote
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + q), j & 1, abort_flag, status)))) break;
       tc_fence_after_sync();
       release(C::B_KEMPTY, j);
       float sv[128];
@@ -394,36 +396,39 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
           tmem_st32(tO + c0 * 32, ov);
         }
       }
-      // P -> e4m3, 16 keys per 16-byte unit, 128-byte-swizzled row of the P tile.
-      float2 se0 = make_float2(0.f, 0.f), se1 = se0;
-      float sr0 = 0.f, sr1 = 0.f, sr2 = 0.f, sr3 = 0.f;
+      // P -> e4m3, 16 keys per 16-byte unit, 128-byte-swizzled row of the P
+      // tile; the row sums follow the hand-off and overlap the P V product.
+      uint32_t pw[32];
 #pragma unroll
       for (int uu = 0; uu < 8; ++uu) {
-        uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = uu * 16 + i * 4;
-          const uint32_t lo = e4m3x2(sv[c], sv[c + 1]);
-          const uint32_t hi = e4m3x2(sv[c + 2], sv[c + 3]);
-          w[i] = lo | (hi << 16);
-          se0 = add2(se0, make_float2(sv[c], sv[c + 1]));
-          se1 = add2(se1, make_float2(sv[c + 2], sv[c + 3]));
-          if (i & 1) {
-            sr2 = add_e4m3x2(sr2, lo);
-            sr3 = add_e4m3x2(sr3, hi);
-          } else {
-            sr0 = add_e4m3x2(sr0, lo);
-            sr1 = add_e4m3x2(sr1, hi);
-          }
+          pw[4 * uu + i] = e4m3x2(sv[c], sv[c + 1]) | (e4m3x2(sv[c + 2], sv[c + 3]) << 16);
         }
-        *reinterpret_cast<uint4*>(prow + ((uu ^ (r & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + ((uu ^ (r & 7)) * 16)) =
+            make_uint4(pw[4 * uu], pw[4 * uu + 1], pw[4 * uu + 2], pw[4 * uu + 3]);
       }
-      l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
-      l_round = l_round * alpha + ((sr0 + sr1) + (sr2 + sr3));
       tmem_st_wait();
       fence_proxy_async_smem();  // P (generic-proxy writes) before the MMA reads it
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL + q));
+      float2 se0 = make_float2(0.f, 0.f), se1 = se0;
+      float sr0 = 0.f, sr1 = 0.f, sr2 = 0.f, sr3 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 4) {
+        se0 = add2(se0, make_float2(sv[c], sv[c + 1]));
+        se1 = add2(se1, make_float2(sv[c + 2], sv[c + 3]));
+      }
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        sr0 = add_e4m3x2(sr0, pw[i] & 0xffffu);
+        sr1 = add_e4m3x2(sr1, pw[i] >> 16);
+        sr2 = add_e4m3x2(sr2, pw[i + 1] & 0xffffu);
+        sr3 = add_e4m3x2(sr3, pw[i + 1] >> 16);
+      }
+      l_exact = l_exact * alpha + ((se0.x + se0.y) + (se1.x + se1.y));
+      l_round = l_round * alpha + ((sr0 + sr1) + (sr2 + sr3));
     }
     if (ok && nk > 0 && mbar_wait(bar(C::B_ODONE + q), (nk - 1) & 1, abort_flag, status)) {
       tc_fence_after_sync();
