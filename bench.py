@@ -233,7 +233,7 @@ def oracle_sample(N, d, causal, seed, heads=1):
     return dt, f + b, threads
 
 
-E2E_CHUNKS = 16  # head-chunks of the pipelined end-to-end step
+E2E_CHUNKS = 8  # head-chunks of the pipelined end-to-end step (4 heads each at B=2 H=16)
 E2E_COMPUTE_STREAMS = 8
 
 DECODE = {"workload": "decode: 1 query token per (b, h) against a bf16 KV cache, B=16 H=16 L=32768 d=128",
@@ -602,10 +602,10 @@ def run_ours(args):
     # chunk c-1's results are copied out (stream s_out).  Every input byte is
     # copied in and every result byte copied out inside the step.
     BH = B * H
-    nch = E2E_CHUNKS if BH % E2E_CHUNKS == 0 else 1
+    nch = args.e2e_chunks if args.e2e_chunks > 0 and BH % args.e2e_chunks == 0 else 1
     hc = BH // nch
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    s_cmp = [torch.cuda.Stream() for _ in range(E2E_COMPUTE_STREAMS)]
+    s_cmp = [torch.cuda.Stream() for _ in range(max(1, args.e2e_streams))]
 
     def flat(t):
         return t.view(BH, *t.shape[2:])
@@ -638,7 +638,7 @@ def run_ours(args):
                 e.record(s_in)
                 ev_in.append(e)
         for c in range(nch):
-            sc = s_cmp[c % E2E_COMPUTE_STREAMS]
+            sc = s_cmp[c % len(s_cmp)]
             sc.wait_event(ev_in[c])
             sl = slice(c * hc, (c + 1) * hc)
             cq, ck, cv, cdo = (dev[n][sl].unsqueeze(0) for n in ("q", "k", "v", "do"))
@@ -737,7 +737,7 @@ def run_ours(args):
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "pipeline": ("%d head-chunks: copies in / compute (%d streams) / copies out overlapped; "
                                      "consecutive steps overlap on two device buffer sets" % (
-                                         nch, E2E_COMPUTE_STREAMS)),
+                                         nch, len(s_cmp))),
                         "sequential_ms_per_step": seq_ms,
                         "sequential_value": world * (f_fwd + f_bwd) / (seq_ms * 1e-3) / 1e12,
                         "outputs_match_device": e2e_check},
@@ -757,6 +757,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=E2E_CHUNKS,
+                    help="head-chunks of the pipelined end-to-end step (must divide B*H, else 1)")
+    ap.add_argument("--e2e-streams", type=int, default=E2E_COMPUTE_STREAMS,
+                    help="compute streams the end-to-end chunks rotate over")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -338,6 +338,28 @@ def test_forward_is_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("d,causal", [(128, False), (128, True), (64, False), (32, True)])
+def test_repeated_runs_bit_identical(d, causal):
+    """The next S is issued right behind the MMA that reads the TMEM columns it
+    overwrites (P V in the forward at d = 128, dV in the backward), relying on
+    the tensor pipe executing one thread's MMAs in issue order.  Were that
+    order ever broken, P (or P^T) would be overwritten while being read, with a
+    timing-dependent result: over a grid of several waves, repeated runs must
+    agree bit for bit in O, LSE, dK and dV (dQ is reduced in arbitrary order),
+    and the first run must match the oracle on sampled rows and columns."""
+    x = make_inputs(AttnShape(2, 8, 2048, d), "bf16", seed=21 + d)
+    s = 1.0 / math.sqrt(d)
+    o0, l0 = gpu_fwd(x, s, causal)
+    g0 = gpu_bwd(x, o0, l0, s, causal)
+    for _ in range(6):
+        o, l = gpu_fwd(x, s, causal)
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    for _ in range(3):
+        g = gpu_bwd(x, o0, l0, s, causal)
+        assert torch.equal(g[1], g0[1]) and torch.equal(g[2], g0[2])
+    _check_sampled(x, s, causal, o0, l0, g0, nrows=64, heads_for_cols=[0, 15], ncols=16)
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_key_shift_invariance_on_gpu(causal):
     """Adding one vector c to every key adds scale * q_i . c to every score of
