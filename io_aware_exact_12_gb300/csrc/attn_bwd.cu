@@ -612,14 +612,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status);
         if (ok && it > 0) ok = mbar_wait(bar(C::B_DQFULL), (it - 1) & 1, abort_flag, status);
         // visit it-1's MMAs are all complete: its Q, dO stage may be refilled
-        if (ok && it > 0 && threadIdx.x == 0) mbar_arrive(bar(C::B_QEMPTY + (it - 1) % C::NSTQ));
+        // (at d <= 64 the dQ warps release it, see there)
+        if (C::DQ_T && ok && it > 0 && threadIdx.x == 0) mbar_arrive(bar(C::B_QEMPTY + (it - 1) % C::NSTQ));
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
       } else {
         if (!(ok = mbar_wait(bar(C::B_DPFULL), it & 1, abort_flag, status))) break;
         if (it > 0 && !(ok = mbar_wait(bar(C::B_DQFULL), (it - 1) & 1, abort_flag, status))) break;
         // visit it-1's MMAs are all complete: its Q, dO stage may be refilled
-        if (it > 0 && threadIdx.x == 0) mbar_arrive(bar(C::B_QEMPTY + (it - 1) % C::NSTQ));
+        // (at d <= 64 the dQ warps release it, see there)
+        if (C::DQ_T && it > 0 && threadIdx.x == 0) mbar_arrive(bar(C::B_QEMPTY + (it - 1) % C::NSTQ));
       }
       tc_fence_after_sync();
       const float2* nd = reinterpret_cast<const float2*>(sDD + s * C::BM + g * 64);  // -D
@@ -741,6 +743,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const int q0 = ATTN_BWD_QTILE(it, qi) * C::BM;
       // warp-uniform (the d <= 64 reductions below shuffle across the warp)
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::B_DQFULL), it & 1, abort_flag, status))) break;
+      // The DQFULL commit follows every MMA of this visit, so the visit's Q, dO
+      // stage is free now.  At d <= 64 this warpgroup, idle until here, hands
+      // it back (the P/dS warps, which do at d = 128, would only see DQFULL at
+      // the next visit's dP wait: +3-5 % measured); at d = 128 the dQ warps
+      // are still reducing the previous visit when DQFULL arrives.
+      if (!C::DQ_T && t == 0) mbar_arrive(bar(C::B_QEMPTY + it % C::NSTQ));
       tc_fence_after_sync();
       uint32_t v[NCOL];
 #pragma unroll
