@@ -339,7 +339,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 
   uint32_t* qbits = reinterpret_cast<uint32_t*>(smem + C::OFF_QBITS);
   int* qcount = reinterpret_cast<int*>(smem + C::OFF_QCOUNT);
-  if (threadIdx.x == 0) {
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
+  // The producer thread sets up the barriers and issues K, V and the first
+  // Q/dO stages before the CTA-wide set-up barrier, so that their load
+  // latency overlaps the TMEM allocation and the barrier itself.
+  int pre_issued = 0;   // visits whose stage loads went out before the barrier
+  int pre_qi = i0 - 1;  // (block-sparse) query-tile cursor after them
+  auto load_stage = [&](int s, int q0) {
+    mbar_arrive_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE_BYTES + 2 * C::VEC_BYTES);
+    for (int c = 0; c < C::NCH; ++c) {
+      tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + s), c * C::CH, q0, bh);
+      tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar(C::B_QFULL + s), c * C::CH, q0, bh);
+    }
+    const int64_t voff = static_cast<int64_t>(bh) * Npad + q0;
+    bulk_load(sbase + C::OFF_LSE + s * C::VEC_BYTES, lse2 + voff, C::VEC_BYTES, bar(C::B_QFULL + s));
+    bulk_load(sbase + C::OFF_DD + s * C::VEC_BYTES, dvec + voff, C::VEC_BYTES, bar(C::B_QFULL + s));
+  };
+  if (warp == 12 && lane == 0) {
     if constexpr (SPARSE) {
       const uint8_t* mb = bmask + static_cast<size_t>((bh % H) % mask_heads) * ntq * ntq;
       int n = 0;
@@ -365,6 +382,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_MMADONE), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_do);
+    mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
+    for (int c = 0; c < C::NCH; ++c) {
+      tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KVFULL), c * C::CH, kv0, bh);
+      tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bar(C::B_KVFULL), c * C::CH, kv0, bh);
+    }
+    pre_issued = min(SPARSE ? *qcount : nq_dense, C::NSTQ);
+    for (int it = 0; it < pre_issued; ++it) {  // stages still empty: no waits
+      const int qt = SPARSE ? (pre_qi = next_set_bit(qbits, pre_qi + 1, ntq)) : i0 + it;
+      load_stage(it, qt * C::BM);
+    }
   }
   if (warp == 13) {
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
@@ -380,40 +411,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   // kept as a plain expression: the cursor form measured 4 % slower there.
 #define ATTN_BWD_QTILE(it, qi) (SPARSE ? ((qi) = next_set_bit(qbits, (qi) + 1, ntq)) : i0 + (it))
 
-  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
-  const uint32_t sQ = sbase + C::OFF_Q, sDO = sbase + C::OFF_DO, sDS = sbase + C::OFF_DS;
 
   if (warp >= 12) {
     regs_decrease<C::REGS_CTRL>();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- producer
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-      prefetch_tensormap(&tm_do);
-      mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::TILE_BYTES);
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KVFULL), c * C::CH, kv0, bh);
-        tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bar(C::B_KVFULL), c * C::CH, kv0, bh);
-      }
-      int issued = 0;
-      int qi = i0 - 1;
-      for (int it = 0; it < nq; ++it) {
+      // (K, V and the first min(NSTQ, nq) stages went out before the set-up
+      // barrier, see above.)
+      int issued = pre_issued;
+      int qi = pre_qi;
+      for (int it = pre_issued; it < nq; ++it) {
         const int s = it % C::NSTQ, u = it / C::NSTQ;
         const int q0 = ATTN_BWD_QTILE(it, qi) * C::BM;
         if (u > 0 && !mbar_wait(bar(C::B_QEMPTY + s), (u - 1) & 1, abort_flag, status)) break;
-        mbar_arrive_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE_BYTES + 2 * C::VEC_BYTES);
-        for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL + s),
-                      c * C::CH, q0, bh);
-          tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar(C::B_QFULL + s),
-                      c * C::CH, q0, bh);
-        }
-        const int64_t voff = static_cast<int64_t>(bh) * Npad + q0;
-        bulk_load(sbase + C::OFF_LSE + s * C::VEC_BYTES, lse2 + voff, C::VEC_BYTES,
-                  bar(C::B_QFULL + s));
-        bulk_load(sbase + C::OFF_DD + s * C::VEC_BYTES, dvec + voff, C::VEC_BYTES,
-                  bar(C::B_QFULL + s));
+        load_stage(s, q0);
         issued = it + 1;
       }
       if (*abort_flag) {

@@ -204,7 +204,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint16_t* pos_tile = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST);
   uint8_t* pos_flags = smem + C::OFF_FLAGS;
   int* npos_slot = reinterpret_cast<int*>(smem + C::OFF_NPOS);
-  if (threadIdx.x == 0) {
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+  // The producer thread sets up the barriers and issues the Q tiles and the
+  // first ring stages before the CTA-wide set-up barrier, so that their load
+  // latency overlaps the TMEM allocation and the barrier itself.
+  int pre_issued = 0;  // positions whose K and V loads went out before the barrier
+  if (warp == 8 && lane == 0) {
     if constexpr (SPARSE) {
       const uint8_t* mb = bmask + static_cast<size_t>((bh % H) % mask_heads) * nkv_all * nkv_all;
       int n = 0, c0 = 0, c1 = 0;
@@ -243,6 +250,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     mbar_init(bar(C::B_MMADONE), 1);
     *abort_flag = 0;
     fence_barrier_init();
+    prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    const int np = SPARSE ? npos_slot[0] : nkv_max;
+    if (np > 0) {  // a CTA with nothing to visit loads nothing
+      mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
+      for (int q = 0; q < 2; ++q)
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sQ + q * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), c * C::CH,
+                      qb * 2 * C::BM + q * C::BM, bh);
+    }
+    pre_issued = min(np, C::NST);
+    for (int j = 0; j < pre_issued; ++j) {  // stages still empty: no waits
+      const int kv_row0 = (SPARSE ? static_cast<int>(pos_tile[j]) : j) * C::BN;
+      mbar_arrive_expect_tx(bar(C::B_KFULL + j), C::TILE_BYTES);
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(sK + j * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bar(C::B_KFULL + j), c * C::CH, kv_row0,
+                    bh);
+      mbar_arrive_expect_tx(bar(C::B_VFULL + j), C::TILE_BYTES);
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(sV + j * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bar(C::B_VFULL + j), c * C::CH, kv_row0,
+                    bh);
+    }
   }
   if (warp == 9) {
     tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
@@ -253,9 +283,6 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t sQ = sbase + C::OFF_Q;
-  const uint32_t sK = sbase + C::OFF_K;
-  const uint32_t sV = sbase + C::OFF_V;
   const int npos = SPARSE ? npos_slot[0] : nkv_max;
   int cnt[2];
   cnt[0] = SPARSE ? npos_slot[1] : nkv[0];
@@ -267,18 +294,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     regs_decrease<C::REGS_CTRL>();
     if (warp == 8 && lane == 0) {
       // ---------------------------------------------------------- producer
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
-      if (npos > 0) {  // a CTA with nothing to visit loads nothing
-        mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
-        for (int q = 0; q < 2; ++q)
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sQ + q * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar(C::B_QFULL), c * C::CH,
-                        qb * 2 * C::BM + q * C::BM, bh);
-      }
-      int issued = 0;
-      for (int j = 0; j < npos; ++j) {
+      // (Q and the first min(NST, npos) positions went out before the set-up
+      // barrier, see above.)
+      int issued = pre_issued;
+      for (int j = pre_issued; j < npos; ++j) {
         const int s = j % C::NST, u = j / C::NST;
         const int kv_row0 = kv_tile(j) * C::BN;
         if (u > 0 && !mbar_wait(bar(C::B_KEMPTY + s), (u - 1) & 1, abort_flag, status)) break;
