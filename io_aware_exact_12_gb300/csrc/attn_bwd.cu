@@ -23,7 +23,9 @@
 // attn_bwd_kernel roles (16 warps = 4 warpgroups, one CTA per SM; warpgroup 3
 // hands registers to warpgroups 0-2 with setmaxnreg: 152, 152, 144 / 64):
 //   * warp 12    : TMA producer: K_j and V_j once; Q_i, dO_i (2-stage ring)
-//                  plus the 128 -LSE*log2e and -D values of tile i (bulk copies).
+//                  plus the 128 -LSE*log2e and -D values of tile i (bulk copies);
+//                  its thread also sets up the barriers and issues K, V and the
+//                  first stages before the CTA's set-up barrier.
 //   * warp 13    : TMEM owner and single-thread tcgen05.mma issuer, per tile i:
 //                    S^T  = K_j Q_i^T          (SS, both K-major)
 //                    dP^T = V_j dO_i^T         (SS, both K-major)
@@ -522,8 +524,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           // One commit tells three parties that dK(i) and dQ(i) (and every
           // MMA before them) are complete: the dQ warps (dQ_i is in TMEM),
           // the P/dS warps (the dS^T tile may be overwritten) and, through
-          // the P/dS warps' arrival, the producer (the Q_i, dO_i stage is
-          // free).  Two tcgen05.commit fewer per visit for the issuing thread.
+          // the arrival of one of them (the P/dS warps at d = 128, the dQ
+          // warps at d <= 64), the producer (the Q_i, dO_i stage is free).
+          // Two tcgen05.commit fewer per visit for the issuing thread.
           tc_commit(bar(C::B_DQFULL));
           ++ik;
           progress = true;

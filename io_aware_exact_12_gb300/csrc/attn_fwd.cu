@@ -15,7 +15,9 @@
 //     softmax warpgroups (setmaxnreg 56 / 224), then:
 //   * warp 8  : TMA producer -- Q0/Q1 once, then K_j and V_j into an
 //               NST-stage ring (128B-swizzled tiles, 3-D tensor maps so a
-//               tile never straddles two heads and rows >= N read as zero).
+//               tile never straddles two heads and rows >= N read as zero);
+//               its thread also sets up the barriers and issues Q and the
+//               first stages before the CTA's set-up barrier.
 //   * warp 9  : TMEM owner and single-thread tcgen05.mma issuer.
 //               S_q = Q_q K_j^T  (SS: both operands K-major in shared memory)
 //               O_q += P_q V_j   (TS: P from TMEM, V MN-major in shared memory)
