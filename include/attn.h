@@ -98,7 +98,8 @@ int attn_bwd_f16(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, void* stream);
 
 /*
- * Forward and backward with dropout fused into the softmax step (bf16;
+ * Forward and backward with dropout fused into the softmax step (bf16, and
+ * fp16 through the _f16 twins below;
  * FlashAttention深度攻略 §7, operator fusion: the softmax step of the fused
  * kernel also applies dropout).  Inverted dropout on P:
  *   t = floor((1 - p_drop) * 256 + 0.5) (in double), the keep probability
@@ -125,9 +126,18 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                      float scale, int causal, float p_drop, unsigned long long seed,
                      unsigned int offset, void* stream);
+/* The same for fp16 q, k, v, o, dO, dq, dk, dv (the keep bytes are identical). */
+int attn_fwd_dropout_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, float p_drop,
+                         unsigned long long seed, unsigned int offset, void* stream);
+int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                         float scale, int causal, float p_drop, unsigned long long seed,
+                         unsigned int offset, void* stream);
 
 /*
- * Block-sparse forward (bf16): attn_fwd where whole 128 x 128 tiles of the
+ * Block-sparse forward (bf16; fp16 through attn_fwd_blocksparse_f16): attn_fwd
+ * where whole 128 x 128 tiles of the
  * score matrix are enabled or skipped by a block mask (FlashAttention深度攻略,
  * 进阶追问 "Sparse FlashAttention"; the tiles skipped are never loaded or
  * multiplied, generalising the causal tile skipping).
@@ -140,9 +150,13 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
 int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
                          const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
                          float scale, int causal, void* stream);
+int attn_fwd_blocksparse_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const unsigned char* block_mask, int mask_heads, int B, int H, int N,
+                             int d, float scale, int causal, void* stream);
 
 /*
- * Block-sparse backward (bf16): the gradients of attn_fwd_blocksparse's output
+ * Block-sparse backward (bf16; fp16 through attn_bwd_blocksparse_f16): the
+ * gradients of attn_fwd_blocksparse's output
  * for the same block_mask, mask_heads and causal flag (o and lse from that
  * call).  The CTA of each 128-key tile visits only the query tiles whose mask
  * entry enables it; a key tile no query tile sees gets dK = dV = 0, and dQ
@@ -153,6 +167,10 @@ int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void
                          const float* lse, void* dq, void* dk, void* dv,
                          const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
                          float scale, int causal, void* stream);
+int attn_bwd_blocksparse_f16(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                             const unsigned char* block_mask, int mask_heads, int B, int H, int N,
+                             int d, float scale, int causal, void* stream);
 
 /*
  * Forward with FP8 (e4m3) inputs: q, k, v are [B, H, N, 128] e4m3 bytes whose

@@ -53,14 +53,18 @@ def lib() -> ctypes.CDLL:
         for f in (L.attn_fwd, L.attn_fwd_f16, L.attn_bwd, L.attn_bwd_f16):
             f.restype = I
         U64, U32 = ctypes.c_ulonglong, ctypes.c_uint
-        L.attn_fwd_dropout.argtypes = [P, P, P, P, P, I, I, I, I, F, I, F, U64, U32, P]
-        L.attn_fwd_dropout.restype = I
-        L.attn_bwd_dropout.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, U64, U32, P]
-        L.attn_bwd_dropout.restype = I
-        L.attn_fwd_blocksparse.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, P]
-        L.attn_fwd_blocksparse.restype = I
-        L.attn_bwd_blocksparse.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P]
-        L.attn_bwd_blocksparse.restype = I
+        for f in (L.attn_fwd_dropout, L.attn_fwd_dropout_f16):
+            f.argtypes = [P, P, P, P, P, I, I, I, I, F, I, F, U64, U32, P]
+            f.restype = I
+        for f in (L.attn_bwd_dropout, L.attn_bwd_dropout_f16):
+            f.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, I, F, U64, U32, P]
+            f.restype = I
+        for f in (L.attn_fwd_blocksparse, L.attn_fwd_blocksparse_f16):
+            f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, P]
+            f.restype = I
+        for f in (L.attn_bwd_blocksparse, L.attn_bwd_blocksparse_f16):
+            f.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P]
+            f.restype = I
         L.attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, F, I, P]
         L.attn_fwd_fp8.restype = I
         L.attn_decode.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
@@ -199,10 +203,10 @@ def attn_bwd(q, k, v, o, do, lse, scale=None, causal=False, dq=None, dk=None, dv
 def attn_fwd_dropout(q, k, v, p_drop, seed, offset=0, scale=None, causal=False, o=None, lse=None, stream=None):
     """attn_fwd with inverted dropout of probability ``p_drop`` on P, the keep
     decisions drawn in the kernel from Philox4x32-10 keyed by ``seed`` (64-bit)
-    with ``offset`` (32-bit) as the fourth counter word.  bf16 only.
+    with ``offset`` (32-bit) as the fourth counter word.  bf16 or fp16.
     Returns (o, lse); lse is that of the undropped softmax."""
     B, H, N, d = _dims(q)
-    _check("q", q, None, torch.bfloat16)
+    _check("q", q)
     _check("k", k, q, q.dtype)
     _check("v", v, q, q.dtype)
     if scale is None:
@@ -213,10 +217,11 @@ def attn_fwd_dropout(q, k, v, p_drop, seed, offset=0, scale=None, causal=False, 
     _check("o", o, q, q.dtype)
     _check("lse", lse, None, torch.float32)
     with _on_device(q):
-        rc = lib().attn_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
-                                    N, d, float(scale), int(bool(causal)), float(p_drop),
-                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
-                                    _stream_handle(stream))
+        fn = lib().attn_fwd_dropout if q.dtype == torch.bfloat16 else lib().attn_fwd_dropout_f16
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
+                N, d, float(scale), int(bool(causal)), float(p_drop),
+                int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                _stream_handle(stream))
     if rc:
         raise AttnError("attn_fwd_dropout", rc)
     return o, lse
@@ -227,7 +232,7 @@ def attn_bwd_dropout(q, k, v, o, do, lse, p_drop, seed, offset=0, scale=None, ca
     """Gradients of attn_fwd_dropout's output (same p_drop, seed, offset): the
     keep decisions are drawn again, not stored.  Returns (dq, dk, dv)."""
     B, H, N, d = _dims(q)
-    _check("q", q, None, torch.bfloat16)
+    _check("q", q)
     for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
         _check(name, t, q, q.dtype)
     _check("lse", lse, None, torch.float32)
@@ -239,11 +244,12 @@ def attn_bwd_dropout(q, k, v, o, do, lse, p_drop, seed, offset=0, scale=None, ca
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(name, t, q, q.dtype)
     with _on_device(q):
-        rc = lib().attn_bwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                                    lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
-                                    float(scale), int(bool(causal)), float(p_drop),
-                                    int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
-                                    _stream_handle(stream))
+        fn = lib().attn_bwd_dropout if q.dtype == torch.bfloat16 else lib().attn_bwd_dropout_f16
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                float(scale), int(bool(causal)), float(p_drop),
+                int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF,
+                _stream_handle(stream))
     if rc:
         raise AttnError("attn_bwd_dropout", rc)
     return dq, dk, dv
@@ -290,22 +296,24 @@ def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, 
     """Forward restricted by a block mask: block_mask is a uint8 CUDA tensor
     [H or 1, ceil(N/128), ceil(N/128)]; key j is visible to query i iff
     block_mask[h][i // 128][j // 128] != 0 (and j <= i if causal).
-    Returns (o, lse); rows that see no key get O = 0, LSE = -inf."""
+    bf16 or fp16.  Returns (o, lse); rows that see no key get O = 0,
+    LSE = -inf."""
     B, H, N, d = _dims(q)
-    _check("q", q, None, torch.bfloat16)
-    _check("k", k, q, torch.bfloat16)
-    _check("v", v, q, torch.bfloat16)
+    _check("q", q)
+    _check("k", k, q, q.dtype)
+    _check("v", v, q, q.dtype)
     _check_block_mask(block_mask, H, N)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     o = torch.empty_like(q) if o is None else o
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check("o", o, q, torch.bfloat16)
+    _check("o", o, q, q.dtype)
     _check("lse", lse, None, torch.float32)
     with _on_device(q):
-        rc = lib().attn_fwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                        block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
-                                        int(bool(causal)), _stream_handle(stream))
+        fn = lib().attn_fwd_blocksparse if q.dtype == torch.bfloat16 else lib().attn_fwd_blocksparse_f16
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
+                int(bool(causal)), _stream_handle(stream))
     if rc:
         raise AttnError("attn_fwd_blocksparse", rc)
     return o, lse
@@ -316,7 +324,7 @@ def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=Fal
     """Gradients of attn_fwd_blocksparse's output for the same block_mask and
     causal flag.  Returns (dq, dk, dv)."""
     B, H, N, d = _dims(q)
-    _check("q", q, None, torch.bfloat16)
+    _check("q", q)
     for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
         _check(name, t, q, q.dtype)
     _check("lse", lse, None, torch.float32)
@@ -329,10 +337,11 @@ def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=Fal
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         _check(name, t, q, q.dtype)
     with _on_device(q):
-        rc = lib().attn_bwd_blocksparse(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                                        block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
-                                        int(bool(causal)), _stream_handle(stream))
+        fn = lib().attn_bwd_blocksparse if q.dtype == torch.bfloat16 else lib().attn_bwd_blocksparse_f16
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
+                int(bool(causal)), _stream_handle(stream))
     if rc:
         raise AttnError("attn_bwd_blocksparse", rc)
     return dq, dk, dv

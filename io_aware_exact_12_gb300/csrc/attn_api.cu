@@ -311,7 +311,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
 
 int blocksparse_entry(const void* q, const void* k, const void* v, void* o, float* lse,
                       const uint8_t* mask, int mask_heads, int B, int H, int N, int d, float scale,
-                      int causal, void* stream) {
+                      int causal, void* stream, bool bf16) {
   if (!mask) return kStatusInvalid;
   if (mask_heads != 1 && mask_heads != H) return kStatusInvalid;
   if ((N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
@@ -336,7 +336,7 @@ int blocksparse_entry(const void* q, const void* k, const void* v, void* o, floa
   a.sl2 = std::fabs(scale) * 1.4426950408889634f;
   a.causal = causal ? 1 : 0;
   a.negate = scale < 0.f ? 1 : 0;
-  a.bf16 = true;
+  a.bf16 = bf16;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = st;
   a.bmask = mask;
@@ -437,6 +437,15 @@ int attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float
   return attn::fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, stream, true, dr);
 }
 
+int attn_fwd_dropout_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, float p_drop,
+                         unsigned long long seed, unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::fwd_entry(q, k, v, o, lse, B, H, N, d, scale, causal, stream, false, dr);
+}
+
 int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
                      const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                      float scale, int causal, float p_drop, unsigned long long seed,
@@ -447,6 +456,16 @@ int attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
   return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, true, dr);
 }
 
+int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                         float scale, int causal, float p_drop, unsigned long long seed,
+                         unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, false, dr);
+}
+
 int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, float descale_k,
                  float descale_v, void* o, float* lse, int B, int H, int N, int d, float scale,
                  int causal, void* stream) {
@@ -454,22 +473,53 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, float descale_q, f
                          stream);
 }
 
+}  // extern "C"
+
+namespace attn {
+namespace {
+int blocksparse_bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                          const float* lse, void* dq, void* dk, void* dv, const unsigned char* block_mask,
+                          int mask_heads, int B, int H, int N, int d, float scale, int causal, void* stream,
+                          bool bf16) {
+  if (!block_mask) return kStatusInvalid;
+  if (mask_heads != 1 && mask_heads != H) return kStatusInvalid;
+  if (N > 0 && (N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+  return bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, bf16, kNoDrop,
+                   block_mask, mask_heads);
+}
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
 int attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o, const void* dO,
                          const float* lse, void* dq, void* dk, void* dv,
                          const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
                          float scale, int causal, void* stream) {
-  if (!block_mask) return attn::kStatusInvalid;
-  if (mask_heads != 1 && mask_heads != H) return attn::kStatusInvalid;
-  if (N > 0 && (N + 127) / 128 > attn::kMaxSparseTiles) return attn::kStatusUnsupported;
-  return attn::bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, true,
-                         attn::kNoDrop, block_mask, mask_heads);
+  return attn::blocksparse_bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, B, H, N, d,
+                                     scale, causal, stream, true);
+}
+
+int attn_bwd_blocksparse_f16(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                             const float* lse, void* dq, void* dk, void* dv,
+                             const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                             float scale, int causal, void* stream) {
+  return attn::blocksparse_bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, B, H, N, d,
+                                     scale, causal, stream, false);
 }
 
 int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
                          const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
                          float scale, int causal, void* stream) {
   return attn::blocksparse_entry(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, scale, causal,
-                                 stream);
+                                 stream, true);
+}
+
+int attn_fwd_blocksparse_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                             const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                             float scale, int causal, void* stream) {
+  return attn::blocksparse_entry(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, scale, causal,
+                                 stream, false);
 }
 
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

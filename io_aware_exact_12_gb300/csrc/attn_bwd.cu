@@ -885,21 +885,20 @@ int launch_bwd_t(const BwdArgs& a) {
 }  // namespace
 
 int launch_bwd(const BwdArgs& a) {
-  if (a.bmask) {  // block-sparse: bf16, no dropout, at most kMaxSparseTiles query tiles
-    if (!a.bf16 || a.drop.t != 0 || (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+  if (a.bmask) {  // block-sparse: no dropout, at most kMaxSparseTiles query tiles
+    if (a.drop.t != 0 || (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
     switch (a.d) {
-      case 32: return launch_bwd_t<32, true, false, true>(a);
-      case 64: return launch_bwd_t<64, true, false, true>(a);
-      case 128: return launch_bwd_t<128, true, false, true>(a);
+      case 32: return a.bf16 ? launch_bwd_t<32, true, false, true>(a) : launch_bwd_t<32, false, false, true>(a);
+      case 64: return a.bf16 ? launch_bwd_t<64, true, false, true>(a) : launch_bwd_t<64, false, false, true>(a);
+      case 128: return a.bf16 ? launch_bwd_t<128, true, false, true>(a) : launch_bwd_t<128, false, false, true>(a);
       default: return kStatusUnsupported;
     }
   }
-  if (a.drop.t != 0) {  // dropout: bf16 only
-    if (!a.bf16) return kStatusUnsupported;
+  if (a.drop.t != 0) {  // dropout
     switch (a.d) {
-      case 32: return launch_bwd_t<32, true, true>(a);
-      case 64: return launch_bwd_t<64, true, true>(a);
-      case 128: return launch_bwd_t<128, true, true>(a);
+      case 32: return a.bf16 ? launch_bwd_t<32, true, true>(a) : launch_bwd_t<32, false, true>(a);
+      case 64: return a.bf16 ? launch_bwd_t<64, true, true>(a) : launch_bwd_t<64, false, true>(a);
+      case 128: return a.bf16 ? launch_bwd_t<128, true, true>(a) : launch_bwd_t<128, false, true>(a);
       default: return kStatusUnsupported;
     }
   }

@@ -864,21 +864,21 @@ int launch_fwd_t(const FwdArgs& a) {
 }  // namespace
 
 int launch_fwd(const FwdArgs& a) {
-  if (a.drop.t != 0) {  // dropout: bf16, dense
-    if (!a.bf16 || a.bmask) return kStatusUnsupported;
+  if (a.drop.t != 0) {  // dropout: dense
+    if (a.bmask) return kStatusUnsupported;
     switch (a.d) {
-      case 32: return launch_fwd_t<32, true, false, true>(a);
-      case 64: return launch_fwd_t<64, true, false, true>(a);
-      case 128: return launch_fwd_t<128, true, false, true>(a);
+      case 32: return a.bf16 ? launch_fwd_t<32, true, false, true>(a) : launch_fwd_t<32, false, false, true>(a);
+      case 64: return a.bf16 ? launch_fwd_t<64, true, false, true>(a) : launch_fwd_t<64, false, false, true>(a);
+      case 128: return a.bf16 ? launch_fwd_t<128, true, false, true>(a) : launch_fwd_t<128, false, false, true>(a);
       default: return kStatusUnsupported;
     }
   }
-  if (a.bmask) {  // block-sparse: bf16 only, at most kMaxSparseTiles key tiles
-    if (!a.bf16 || (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+  if (a.bmask) {  // block-sparse: at most kMaxSparseTiles key tiles
+    if ((a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
     switch (a.d) {
-      case 32: return launch_fwd_t<32, true, true>(a);
-      case 64: return launch_fwd_t<64, true, true>(a);
-      case 128: return launch_fwd_t<128, true, true>(a);
+      case 32: return a.bf16 ? launch_fwd_t<32, true, true>(a) : launch_fwd_t<32, false, true>(a);
+      case 64: return a.bf16 ? launch_fwd_t<64, true, true>(a) : launch_fwd_t<64, false, true>(a);
+      case 128: return a.bf16 ? launch_fwd_t<128, true, true>(a) : launch_fwd_t<128, false, true>(a);
       default: return kStatusUnsupported;
     }
   }

@@ -39,8 +39,15 @@ def _random_mask(heads, nb, density, seed, keep_diag=True):
     return m
 
 
-def _check(pkg, shape, mask, causal, seed, scale=None):
-    x = make_inputs(shape, "bf16", seed=seed, with_grad=False)
+def _half_ulp(ref, dtype):
+    if dtype == torch.bfloat16:
+        return _half_ulp_bf16(ref)
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 1e-30)))
+    return np.exp2(np.maximum(e, -14) - 11)
+
+
+def _check(pkg, shape, mask, causal, seed, scale=None, dtype="bf16"):
+    x = make_inputs(shape, dtype, seed=seed, with_grad=False)
     scale = 1.0 / math.sqrt(shape.d) if scale is None else scale
     o, lse = pkg.attn_fwd_blocksparse(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), mask.cuda(), scale=scale,
                                       causal=causal)
@@ -52,7 +59,7 @@ def _check(pkg, shape, mask, causal, seed, scale=None):
     assert np.array_equal(np.isneginf(gl), empty)            # the same rows see no key
     assert (go[empty] == 0).all()
     err = np.abs(go - oo)
-    assert (err - _half_ulp_bf16(oo)).max() <= 1e-2, "max|dO| %g" % err.max()
+    assert (err - _half_ulp(oo, o.dtype)).max() <= 1e-2, "max|dO| %g" % err.max()
     assert np.abs(gl[~empty] - lo[~empty]).max() <= 1e-3
     return o, lse
 
@@ -121,8 +128,8 @@ def test_sparse_long_sequence_sampled_rows(pkg):
 # denominator floored at 1e-3 |dO| where an exact gradient vanishes); key
 # tiles no query tile sees must have dK = dV = 0 exactly, and query blocks that
 # see no key dQ = 0 exactly.
-def _check_bwd(pkg, shape, mask, causal, seed, scale=None):
-    x = make_inputs(shape, "bf16", seed=seed)
+def _check_bwd(pkg, shape, mask, causal, seed, scale=None, dtype="bf16"):
+    x = make_inputs(shape, dtype, seed=seed)
     scale = 1.0 / math.sqrt(shape.d) if scale is None else scale
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     m = mask.cuda()
@@ -198,3 +205,15 @@ def test_backward_sparse_longer_sequence(pkg):
     N, nb = 4096, 32
     for causal in (False, True):
         _check_bwd(pkg, AttnShape(1, 2, N, 128), _random_mask(2, nb, 0.25, seed=21 + causal), causal, seed=22)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N,d", [(1000, 128), (300, 32)])
+def test_fp16_random_block_masks_forward_and_backward(pkg, N, d, causal):
+    """The fp16 twins of the block-sparse forward and backward."""
+    nb = (N + 127) // 128
+    mask = _random_mask(3, nb, 0.4, seed=N + d + 7)
+    o, _ = _check(pkg, AttnShape(2, 3, N, d), mask, causal, seed=N + 3, dtype="fp16")
+    assert o.dtype == torch.float16
+    dq, dk, dv = _check_bwd(pkg, AttnShape(2, 3, N, d), mask, causal, seed=N + 4, dtype="fp16")
+    assert dq.dtype == torch.float16

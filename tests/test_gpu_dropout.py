@@ -59,6 +59,14 @@ def half_ulp_bf16(ref):
     return np.exp2(e - 8)
 
 
+def half_ulp(ref, dtype):
+    """Half an ulp of the output format (bf16 or fp16) at the exact value."""
+    if dtype == torch.bfloat16:
+        return half_ulp_bf16(ref)
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 1e-30)))
+    return np.exp2(np.maximum(e, -14) - 11)
+
+
 def rel_fro(a, b, floor=1e-30):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), floor))
 
@@ -82,11 +90,11 @@ def check_full(x, scale, causal, drop, o, lse, grads):
     q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
     oo, lo, P = oracle.forward(q, k, v, scale, causal, want_p=True, dropout=d32)
     err = np.abs(f64(o) - oo)
-    assert (err - half_ulp_bf16(oo)).max() <= TOL_O, "max|dO| %g" % err.max()
+    assert (err - half_ulp(oo, o.dtype)).max() <= TOL_O, "max|dO| %g" % err.max()
     assert np.abs(f64(lse) - lo).max() <= TOL_LSE
     ref = oracle.backward(q, k, v, oo, do, scale, causal, dropout=d32)
     floor = 1e-3 * float(np.linalg.norm(do))
-    delta = (np.abs(do) * 2 * half_ulp_bf16(oo)).sum(-1)  # [B, H, N]
+    delta = (np.abs(do) * 2 * half_ulp(oo, o.dtype)).sum(-1)  # [B, H, N]
     extra = {"dq": abs(scale) * delta[..., None] * (P @ np.abs(k)),
              "dk": abs(scale) * np.einsum("bhij,bhi,bhic->bhjc", P, delta, np.abs(q)),
              "dv": np.zeros_like(do)}
@@ -112,6 +120,18 @@ def test_ragged_full(N, d):
     for causal in (False, True):
         drop = (0.2, 77 + N, d)
         o, lse, grads = run(x, 1 / math.sqrt(d), causal, drop)
+        check_full(x, 1 / math.sqrt(d), causal, drop, o, lse, grads)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_fp16_full(d):
+    """The fp16 twins: the same keep decisions (the draws do not depend on the
+    input type), parity with the oracle on fp16-rounded inputs."""
+    x = make_inputs(AttnShape(2, 3, 300, d), "fp16", seed=40 + d)
+    for causal in (False, True):
+        drop = (0.15, 0xC0FFEE + d, 5)
+        o, lse, grads = run(x, 1 / math.sqrt(d), causal, drop)
+        assert o.dtype == torch.float16 and grads[0].dtype == torch.float16
         check_full(x, 1 / math.sqrt(d), causal, drop, o, lse, grads)
 
 
@@ -230,5 +250,7 @@ def test_bad_probability_is_rejected():
     for p in (1.0, -0.5, float("nan"), 0.999):
         with pytest.raises(pkg.AttnError):
             pkg.attn_fwd_dropout(q, k, v, p, 1, 0)
-    with pytest.raises(TypeError):
-        pkg.attn_fwd_dropout(q.half(), k.half(), v.half(), 0.1, 1, 0)
+    with pytest.raises(TypeError):  # bf16 or fp16 only
+        pkg.attn_fwd_dropout(q.float(), k.float(), v.float(), 0.1, 1, 0)
+    with pytest.raises(TypeError):  # one type for all inputs
+        pkg.attn_fwd_dropout(q, k.half(), v, 0.1, 1, 0)
