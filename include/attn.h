@@ -145,7 +145,8 @@ int attn_bwd_dropout_f16(const void* q, const void* k, const void* v, const void
  *                head h uses mask (h % H) % mask_heads, mask_heads in {1, H}.
  *                Key j is visible to query i iff
  *                block_mask[..][i / 128][j / 128] != 0 (and j <= i if causal).
- *   A row that sees no key gets O = 0 and LSE = -inf.  N <= 65536.
+ *   A row that sees no key gets O = 0 and LSE = -inf.  N <= 262144 (else
+ *   ATTN_ERR_UNSUPPORTED).
  */
 int attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o, float* lse,
                          const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,

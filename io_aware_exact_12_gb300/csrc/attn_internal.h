@@ -21,8 +21,10 @@ constexpr int kStatusTimeout = 4;
 constexpr int kStatusArch = 5;
 constexpr int kStatusDeviceCheck = 6;
 
-// Block-sparse forward: at most this many 128-key tiles (N <= 65536).
-constexpr int kMaxSparseTiles = 512;
+// Block-sparse: at most this many 128-row tiles (N <= 262144); the forward
+// keeps a 3-byte entry per key tile and the backward a bit per query tile in
+// shared memory.
+constexpr int kMaxSparseTiles = 2048;
 
 // Dropout fused into the softmax step (t == 0: off).  Element (i, j) of head
 // bh is kept iff a Philox byte drawn for it is below t; kept probabilities

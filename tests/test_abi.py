@@ -128,4 +128,4 @@ def test_blocksparse_backward_rejects_bad_arguments(L):
     a = [FAKE + i * 0x100000 for i in range(9)]
     assert L.attn_bwd_blocksparse(*a, None, 1, 1, 2, 256, 128, 0.1, 0, None) == 1       # no mask
     assert L.attn_bwd_blocksparse(*a, FAKE, 3, 1, 2, 256, 128, 0.1, 0, None) == 1       # mask_heads not 1 or H
-    assert L.attn_bwd_blocksparse(*a, FAKE, 1, 1, 2, 65536 + 128, 128, 0.1, 0, None) == 2  # > 512 tiles
+    assert L.attn_bwd_blocksparse(*a, FAKE, 1, 1, 2, 262144 + 128, 128, 0.1, 0, None) == 2  # > 2048 tiles

@@ -200,6 +200,38 @@ def test_backward_all_ones_mask_equals_dense(pkg):
         assert (g1[0].float() - g2[0].float()).abs().max().item() <= 1e-2 * g1[0].float().abs().max().item()
 
 
+def test_sparse_beyond_512_tiles(pkg):
+    """N = 66176 (517 key tiles, past the former 512-tile limit), a 4 %-dense
+    mask: sampled forward rows against the oracle on each row's visible keys;
+    the backward runs, and key tiles no query tile sees get dK = dV = 0."""
+    N, d = 66176, 64
+    nb = (N + 127) // 128
+    mask = _random_mask(1, nb, 0.04, seed=31)
+    mask[0, :, 515] = 0                        # one key tile nobody sees
+    x = make_inputs(AttnShape(1, 1, N, d), "bf16", seed=32)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    m = mask.cuda()
+    o, lse = pkg.attn_fwd_blocksparse(q, k, v, m, scale=1 / math.sqrt(d), causal=False)
+    assert pkg.sync_status() == 0
+    rng = np.random.default_rng(3)
+    for i in list(rng.integers(0, N, 12)) + [N - 1]:
+        cols = np.concatenate([np.arange(j * 128, min(N, j * 128 + 128)) for j in range(nb) if mask[0, i // 128, j]])
+        L = len(cols)
+        qq = np.zeros((1, 1, L, d))
+        qq[0, 0, L - 1] = x["q"][0, 0, i].double().numpy()
+        ro, rl, _ = oracle.rows(qq, x["k"][0, 0].double().numpy()[cols][None, None],
+                                x["v"][0, 0].double().numpy()[cols][None, None], None, 1 / math.sqrt(d), False,
+                                np.array([0]), np.array([L - 1]))
+        go = o[0, 0, i].double().cpu().numpy()
+        assert (np.abs(go - ro[0]) - _half_ulp_bf16(ro[0])).max() <= 1e-2
+        assert abs(lse[0, 0, i].item() - rl[0]) <= 1e-3
+    dq, dk, dv = pkg.attn_bwd_blocksparse(q, k, v, o, do, lse, m, scale=1 / math.sqrt(d), causal=False)
+    assert pkg.sync_status() == 0
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    assert not dk[0, 0, 515 * 128:516 * 128].any() and not dv[0, 0, 515 * 128:516 * 128].any()
+    assert dk[0, 0, 514 * 128:515 * 128].any() or not mask[0, :, 514].any()
+
+
 def test_backward_sparse_longer_sequence(pkg):
     """N = 4096, 25 %-dense per-head masks, causal and not, against the full oracle."""
     N, nb = 4096, 32
