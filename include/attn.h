@@ -174,6 +174,36 @@ int attn_bwd_blocksparse_f16(const void* q, const void* k, const void* v, const 
                              int d, float scale, int causal, void* stream);
 
 /*
+ * Block-sparse attention with dropout (both passes; bf16, fp16 through the
+ * _f16 twins): the block mask of attn_fwd_blocksparse decides which keys a
+ * query sees, and among those the keep rule of attn_fwd_dropout applies
+ * unchanged -- keep_ij depends only on (i, j, b * H + h, seed, offset), not on
+ * the mask (FlashAttention深度攻略 §7 fuses mask and dropout into the one
+ * softmax step; 进阶追问 "Sparse FlashAttention" skips the masked tiles).
+ * Arguments are those of attn_fwd_blocksparse / attn_bwd_blocksparse followed
+ * by p_drop, seed and offset as for attn_fwd_dropout; the errors are the
+ * union of both.  t = 256 runs the block-sparse kernels without dropout.
+ */
+int attn_fwd_blocksparse_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                                 float scale, int causal, float p_drop, unsigned long long seed,
+                                 unsigned int offset, void* stream);
+int attn_fwd_blocksparse_dropout_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const unsigned char* block_mask, int mask_heads, int B, int H, int N,
+                                     int d, float scale, int causal, float p_drop, unsigned long long seed,
+                                     unsigned int offset, void* stream);
+int attn_bwd_blocksparse_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                 const float* lse, void* dq, void* dk, void* dv,
+                                 const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                                 float scale, int causal, float p_drop, unsigned long long seed,
+                                 unsigned int offset, void* stream);
+int attn_bwd_blocksparse_dropout_f16(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                     const unsigned char* block_mask, int mask_heads, int B, int H, int N,
+                                     int d, float scale, int causal, float p_drop, unsigned long long seed,
+                                     unsigned int offset, void* stream);
+
+/*
  * Forward with FP8 (e4m3) inputs: q, k, v are [B, H, N, 128] e4m3 bytes whose
  * real values are descale_q*q, descale_k*k, descale_v*v (per-tensor factors,
  * finite and > 0); o is bf16 [B, H, N, 128], lse fp32 [B, H, N] in the units

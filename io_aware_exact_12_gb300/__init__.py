@@ -19,7 +19,8 @@ import os
 
 import torch
 
-__all__ = ["attention", "attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_bwd_blocksparse", "sync_status", "status_string", "last_launch_count", "lib",
+__all__ = ["attention", "attn_fwd", "attn_bwd", "attn_fwd_dropout", "attn_bwd_dropout", "attn_decode", "attn_fwd_fp8", "attn_fwd_blocksparse", "attn_bwd_blocksparse",
+           "attn_fwd_blocksparse_dropout", "attn_bwd_blocksparse_dropout", "sync_status", "status_string", "last_launch_count", "lib",
            "AttnError", "LIB_PATH", "STATUS"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
@@ -64,6 +65,12 @@ def lib() -> ctypes.CDLL:
             f.restype = I
         for f in (L.attn_bwd_blocksparse, L.attn_bwd_blocksparse_f16):
             f.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, P]
+            f.restype = I
+        for f in (L.attn_fwd_blocksparse_dropout, L.attn_fwd_blocksparse_dropout_f16):
+            f.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, I, F, U64, U32, P]
+            f.restype = I
+        for f in (L.attn_bwd_blocksparse_dropout, L.attn_bwd_blocksparse_dropout_f16):
+            f.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, F, U64, U32, P]
             f.restype = I
         L.attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, F, I, P]
         L.attn_fwd_fp8.restype = I
@@ -292,12 +299,7 @@ def _check_block_mask(block_mask, H, N):
         raise ValueError("block_mask must be a contiguous uint8 CUDA tensor [H or 1, %d, %d]" % (nb, nb))
 
 
-def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, lse=None, stream=None):
-    """Forward restricted by a block mask: block_mask is a uint8 CUDA tensor
-    [H or 1, ceil(N/128), ceil(N/128)]; key j is visible to query i iff
-    block_mask[h][i // 128][j // 128] != 0 (and j <= i if causal).
-    bf16 or fp16.  Returns (o, lse); rows that see no key get O = 0,
-    LSE = -inf."""
+def _fwd_blocksparse(name, q, k, v, block_mask, scale, causal, o, lse, stream, drop=None):
     B, H, N, d = _dims(q)
     _check("q", q)
     _check("k", k, q, q.dtype)
@@ -309,24 +311,24 @@ def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, 
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check("o", o, q, q.dtype)
     _check("lse", lse, None, torch.float32)
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale), int(bool(causal))]
+    if drop is not None:
+        p_drop, seed, offset = drop
+        args += [float(p_drop), int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF]
     with _on_device(q):
-        fn = lib().attn_fwd_blocksparse if q.dtype == torch.bfloat16 else lib().attn_fwd_blocksparse_f16
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
-                int(bool(causal)), _stream_handle(stream))
+        fn = getattr(lib(), name if q.dtype == torch.bfloat16 else name + "_f16")
+        rc = fn(*args, _stream_handle(stream))
     if rc:
-        raise AttnError("attn_fwd_blocksparse", rc)
+        raise AttnError(name, rc)
     return o, lse
 
 
-def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=False, dq=None, dk=None, dv=None,
-                         stream=None):
-    """Gradients of attn_fwd_blocksparse's output for the same block_mask and
-    causal flag.  Returns (dq, dk, dv)."""
+def _bwd_blocksparse(name, q, k, v, o, do, lse, block_mask, scale, causal, dq, dk, dv, stream, drop=None):
     B, H, N, d = _dims(q)
     _check("q", q)
-    for name, t in (("k", k), ("v", v), ("o", o), ("do", do)):
-        _check(name, t, q, q.dtype)
+    for n, t in (("k", k), ("v", v), ("o", o), ("do", do)):
+        _check(n, t, q, q.dtype)
     _check("lse", lse, None, torch.float32)
     _check_block_mask(block_mask, H, N)
     if scale is None:
@@ -334,17 +336,54 @@ def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=Fal
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check(name, t, q, q.dtype)
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check(n, t, q, q.dtype)
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), block_mask.data_ptr(), int(block_mask.shape[0]),
+            B, H, N, d, float(scale), int(bool(causal))]
+    if drop is not None:
+        p_drop, seed, offset = drop
+        args += [float(p_drop), int(seed) & 0xFFFFFFFFFFFFFFFF, int(offset) & 0xFFFFFFFF]
     with _on_device(q):
-        fn = lib().attn_bwd_blocksparse if q.dtype == torch.bfloat16 else lib().attn_bwd_blocksparse_f16
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                block_mask.data_ptr(), int(block_mask.shape[0]), B, H, N, d, float(scale),
-                int(bool(causal)), _stream_handle(stream))
+        fn = getattr(lib(), name if q.dtype == torch.bfloat16 else name + "_f16")
+        rc = fn(*args, _stream_handle(stream))
     if rc:
-        raise AttnError("attn_bwd_blocksparse", rc)
+        raise AttnError(name, rc)
     return dq, dk, dv
+
+
+def attn_fwd_blocksparse(q, k, v, block_mask, scale=None, causal=False, o=None, lse=None, stream=None):
+    """Forward restricted by a block mask: block_mask is a uint8 CUDA tensor
+    [H or 1, ceil(N/128), ceil(N/128)]; key j is visible to query i iff
+    block_mask[h][i // 128][j // 128] != 0 (and j <= i if causal).
+    bf16 or fp16.  Returns (o, lse); rows that see no key get O = 0,
+    LSE = -inf."""
+    return _fwd_blocksparse("attn_fwd_blocksparse", q, k, v, block_mask, scale, causal, o, lse, stream)
+
+
+def attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=None, causal=False, dq=None, dk=None, dv=None,
+                         stream=None):
+    """Gradients of attn_fwd_blocksparse's output for the same block_mask and
+    causal flag.  Returns (dq, dk, dv)."""
+    return _bwd_blocksparse("attn_bwd_blocksparse", q, k, v, o, do, lse, block_mask, scale, causal, dq, dk, dv,
+                            stream)
+
+
+def attn_fwd_blocksparse_dropout(q, k, v, block_mask, p_drop, seed, offset=0, scale=None, causal=False, o=None,
+                                 lse=None, stream=None):
+    """attn_fwd_blocksparse with the dropout of attn_fwd_dropout on the keys
+    the mask leaves visible (the keep decisions do not depend on the mask).
+    Returns (o, lse); lse is that of the undropped softmax."""
+    return _fwd_blocksparse("attn_fwd_blocksparse_dropout", q, k, v, block_mask, scale, causal, o, lse, stream,
+                            (p_drop, seed, offset))
+
+
+def attn_bwd_blocksparse_dropout(q, k, v, o, do, lse, block_mask, p_drop, seed, offset=0, scale=None,
+                                 causal=False, dq=None, dk=None, dv=None, stream=None):
+    """Gradients of attn_fwd_blocksparse_dropout's output (same mask, causal
+    flag, p_drop, seed, offset).  Returns (dq, dk, dv)."""
+    return _bwd_blocksparse("attn_bwd_blocksparse_dropout", q, k, v, o, do, lse, block_mask, scale, causal,
+                            dq, dk, dv, stream, (p_drop, seed, offset))
 
 
 def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, scale=None, causal=False, o=None, lse=None,
@@ -374,41 +413,54 @@ def attn_fwd_fp8(q, k, v, descale_q, descale_k, descale_v, scale=None, causal=Fa
 
 
 class _Attention(torch.autograd.Function):
-    """Differentiable exact attention: forward through attn_fwd (or
-    attn_fwd_dropout), backward through attn_bwd (or attn_bwd_dropout) from
-    the saved O and LSE (P is recomputed, never stored)."""
+    """Differentiable exact attention: forward through attn_fwd (or its
+    dropout / block-mask variants), backward through the matching attn_bwd*
+    from the saved O and LSE (P is recomputed, never stored)."""
 
     @staticmethod
-    def forward(ctx, q, k, v, scale, causal, p_drop, seed, offset):
+    def forward(ctx, q, k, v, scale, causal, p_drop, seed, offset, block_mask):
         q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-        if p_drop > 0.0:
+        if block_mask is not None and p_drop > 0.0:
+            o, lse = attn_fwd_blocksparse_dropout(q, k, v, block_mask, p_drop, seed, offset, scale=scale,
+                                                  causal=causal)
+        elif block_mask is not None:
+            o, lse = attn_fwd_blocksparse(q, k, v, block_mask, scale=scale, causal=causal)
+        elif p_drop > 0.0:
             o, lse = attn_fwd_dropout(q, k, v, p_drop, seed, offset, scale=scale, causal=causal)
         else:
             o, lse = attn_fwd(q, k, v, scale=scale, causal=causal)
         ctx.save_for_backward(q, k, v, o, lse)
-        ctx.args = (scale, causal, p_drop, seed, offset)
+        ctx.args = (scale, causal, p_drop, seed, offset, block_mask)
         return o
 
     @staticmethod
     def backward(ctx, do):
         q, k, v, o, lse = ctx.saved_tensors
-        scale, causal, p_drop, seed, offset = ctx.args
+        scale, causal, p_drop, seed, offset, block_mask = ctx.args
         do = do.contiguous()
-        if p_drop > 0.0:
+        if block_mask is not None and p_drop > 0.0:
+            dq, dk, dv = attn_bwd_blocksparse_dropout(q, k, v, o, do, lse, block_mask, p_drop, seed, offset,
+                                                      scale=scale, causal=causal)
+        elif block_mask is not None:
+            dq, dk, dv = attn_bwd_blocksparse(q, k, v, o, do, lse, block_mask, scale=scale, causal=causal)
+        elif p_drop > 0.0:
             dq, dk, dv = attn_bwd_dropout(q, k, v, o, do, lse, p_drop, seed, offset, scale=scale, causal=causal)
         else:
             dq, dk, dv = attn_bwd(q, k, v, o, do, lse, scale=scale, causal=causal)
-        return dq, dk, dv, None, None, None, None, None
+        return dq, dk, dv, None, None, None, None, None, None
 
 
-def attention(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0):
+def attention(q, k, v, scale=None, causal=False, dropout_p=0.0, seed=0, offset=0, block_mask=None):
     """O = softmax(scale q k^T [+ causal mask]) v as a differentiable op on
-    [B, H, N, d] CUDA tensors (bf16/fp16; with dropout, bf16).  Gradients
-    flow to q, k and v through the recomputation backward.  With dropout_p > 0
-    the keep decisions come from (seed, offset); use a new offset per step."""
+    [B, H, N, d] CUDA tensors (bf16 or fp16).  Gradients flow to q, k and v
+    through the recomputation backward.  With dropout_p > 0 the keep
+    decisions come from (seed, offset); use a new offset per step.  With a
+    block_mask (uint8 [H or 1, ceil(N/128), ceil(N/128)] on the device) only
+    the enabled 128 x 128 tiles are computed, as in attn_fwd_blocksparse."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
-    return _Attention.apply(q, k, v, float(scale), bool(causal), float(dropout_p), int(seed), int(offset))
+    return _Attention.apply(q, k, v, float(scale), bool(causal), float(dropout_p), int(seed), int(offset),
+                            block_mask)
 
 
 def sync_status(stream=None) -> int:

@@ -311,7 +311,7 @@ int bwd_entry(const void* q, const void* k, const void* v, const void* o, const 
 
 int blocksparse_entry(const void* q, const void* k, const void* v, void* o, float* lse,
                       const uint8_t* mask, int mask_heads, int B, int H, int N, int d, float scale,
-                      int causal, void* stream, bool bf16) {
+                      int causal, void* stream, bool bf16, const DropParams& drop = kNoDrop) {
   if (!mask) return kStatusInvalid;
   if (mask_heads != 1 && mask_heads != H) return kStatusInvalid;
   if ((N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
@@ -342,6 +342,7 @@ int blocksparse_entry(const void* q, const void* k, const void* v, void* o, floa
   a.bmask = mask;
   a.H = H;
   a.mask_heads = mask_heads;
+  a.drop = drop;
   rc = launch_fwd(a);
   if (rc == kStatusOk) t_last_launches = 1;
   return rc;
@@ -480,11 +481,11 @@ namespace {
 int blocksparse_bwd_entry(const void* q, const void* k, const void* v, const void* o, const void* dO,
                           const float* lse, void* dq, void* dk, void* dv, const unsigned char* block_mask,
                           int mask_heads, int B, int H, int N, int d, float scale, int causal, void* stream,
-                          bool bf16) {
+                          bool bf16, const DropParams& drop = kNoDrop) {
   if (!block_mask) return kStatusInvalid;
   if (mask_heads != 1 && mask_heads != H) return kStatusInvalid;
   if (N > 0 && (N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
-  return bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, bf16, kNoDrop,
+  return bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, stream, bf16, drop,
                    block_mask, mask_heads);
 }
 }  // namespace
@@ -520,6 +521,52 @@ int attn_fwd_blocksparse_f16(const void* q, const void* k, const void* v, void* 
                              float scale, int causal, void* stream) {
   return attn::blocksparse_entry(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, scale, causal,
                                  stream, false);
+}
+
+int attn_fwd_blocksparse_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                                 float scale, int causal, float p_drop, unsigned long long seed,
+                                 unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::blocksparse_entry(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, scale, causal,
+                                 stream, true, dr);
+}
+
+int attn_fwd_blocksparse_dropout_f16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                     const unsigned char* block_mask, int mask_heads, int B, int H, int N,
+                                     int d, float scale, int causal, float p_drop, unsigned long long seed,
+                                     unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::blocksparse_entry(q, k, v, o, lse, block_mask, mask_heads, B, H, N, d, scale, causal,
+                                 stream, false, dr);
+}
+
+int attn_bwd_blocksparse_dropout(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                                 const float* lse, void* dq, void* dk, void* dv,
+                                 const unsigned char* block_mask, int mask_heads, int B, int H, int N, int d,
+                                 float scale, int causal, float p_drop, unsigned long long seed,
+                                 unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::blocksparse_bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, B, H, N, d,
+                                     scale, causal, stream, true, dr);
+}
+
+int attn_bwd_blocksparse_dropout_f16(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                                     const unsigned char* block_mask, int mask_heads, int B, int H, int N,
+                                     int d, float scale, int causal, float p_drop, unsigned long long seed,
+                                     unsigned int offset, void* stream) {
+  attn::DropParams dr;
+  const int rc = attn::make_drop(p_drop, seed, offset, &dr);
+  if (rc) return rc;
+  return attn::blocksparse_bwd_entry(q, k, v, o, dO, lse, dq, dk, dv, block_mask, mask_heads, B, H, N, d,
+                                     scale, causal, stream, false, dr);
 }
 
 int attn_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -576,7 +576,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
       }
     };
-    if (DROP && nq > 0) draw_visit(i0 * C::BM + g * 64);  // dropout is dense: visit it is tile i0 + it
+    // the query tile of the first visit: i0, or (SPARSE) the first the mask enables
+    if (DROP && nq > 0) draw_visit((SPARSE ? next_set_bit(qbits, i0, ntq) : i0) * C::BM + g * 64);
     for (int it = 0; it < nq; ++it) {
       const int s = it % C::NSTQ;
       const int q0 = ATTN_BWD_QTILE(it, qi) * C::BM + g * 64;  // first query of this thread's half
@@ -672,7 +673,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       fence_proxy_async_smem();
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_DSFULL));
-      if (DROP && it + 1 < nq) draw_visit(q0 + C::BM);
+      if (DROP && it + 1 < nq)  // the next visit's query tile (qi: this visit's under SPARSE)
+        draw_visit(SPARSE ? next_set_bit(qbits, qi + 1, ntq) * C::BM + g * 64 : q0 + C::BM);
     }
     // dK (warpgroup 0) or dV (warpgroup 1) once the last MMAs have completed.
     // At d = 128 the rows leave through the K (dK) or V (dV) tile in shared
@@ -885,8 +887,17 @@ int launch_bwd_t(const BwdArgs& a) {
 }  // namespace
 
 int launch_bwd(const BwdArgs& a) {
-  if (a.bmask) {  // block-sparse: no dropout, at most kMaxSparseTiles query tiles
-    if (a.drop.t != 0 || (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+  if (a.bmask && a.drop.t != 0) {  // block-sparse with dropout
+    if ((a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+    switch (a.d) {
+      case 32: return a.bf16 ? launch_bwd_t<32, true, true, true>(a) : launch_bwd_t<32, false, true, true>(a);
+      case 64: return a.bf16 ? launch_bwd_t<64, true, true, true>(a) : launch_bwd_t<64, false, true, true>(a);
+      case 128: return a.bf16 ? launch_bwd_t<128, true, true, true>(a) : launch_bwd_t<128, false, true, true>(a);
+      default: return kStatusUnsupported;
+    }
+  }
+  if (a.bmask) {  // block-sparse: at most kMaxSparseTiles query tiles
+    if ((a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
     switch (a.d) {
       case 32: return a.bf16 ? launch_bwd_t<32, true, false, true>(a) : launch_bwd_t<32, false, false, true>(a);
       case 64: return a.bf16 ? launch_bwd_t<64, true, false, true>(a) : launch_bwd_t<64, false, false, true>(a);

@@ -45,6 +45,8 @@
 // waiting for this tile's S; the P V product starts on keys 0-63 while the
 // second half is masked, and the epilogue folds 256 / t into 1 / l.  m, l and
 // LSE stay those of the undropped softmax.
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "dropout.cuh"
 #include "tc_sm103.cuh"
@@ -455,6 +457,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         int sp[2] = {0, 0};  // next position to consider for S, per tile
         int pp[2] = {0, 0};  // next position to consider for PV, per tile
         int ns[2] = {0, 0}, np[2] = {0, 0};  // S / PV groups issued per tile
+        bool half[2] = {false, false};       // dropout: keys 0-63 of PV_q issued, 64-127 not yet
         int k_ready = 0, v_ready = 0;  // positions whose K / V load has been seen to land
         int k_rel = 0, v_rel = 0;      // next position whose K / V stage is still held
         IdleWatch watch;
@@ -473,9 +476,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             while (sp[q] < npos && !uses(q, sp[q])) ++sp[q];
             while (pp[q] < sp[q] && !uses(q, pp[q])) ++pp[q];
             // PV_q at pp (its S was issued: every used position below sp has one)
+            // (with dropout in two halves, as in the dense issuer: keys 0-63
+            // once that half of P is written, keys 64-127 once all of it is)
             const int jv = pp[q];
-            if (jv < sp[q] && jv < v_ready && mbar_probe(bar(C::B_PFULL + q), np[q] & 1)) {
-              tc_fence_after_sync();
+            using KK_FIRST = std::integral_constant<int, DROP ? C::BN / 32 : C::BN / 16>;
+            using KK_ALL = std::integral_constant<int, C::BN / 16>;
+            auto issue_pv = [&](auto kk0c, auto kk1c) {  // MMA groups [kk0, kk1) of 16 keys
+              constexpr int kk0 = decltype(kk0c)::value, kk1 = decltype(kk1c)::value;
               const uint32_t d_o = tmem + C::TM_O + q * D;
               const uint32_t a_p = tmem + C::TM_P + q * C::TM_PSTRIDE;
               // (descriptor words at d <= 64; at d = 128 this issuer measured 9 %
@@ -483,18 +490,36 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               if constexpr (C::SEPP) {
                 const uint32_t v_lo = smem_desc_lo(sV + (jv % C::NST) * C::TILE_BYTES, C::CHUNK_BYTES);
   #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
+                for (int kk = kk0; kk < kk1; ++kk)
                   mma_ts_w(d_o, a_p + kk * 8, v_lo + mnmajor_lo_step<D>(kk), HI, idesc_o,
                            (np[q] > 0 || kk > 0) ? 1u : 0u);
               } else {
                 const uint32_t v_s = sV + (jv % C::NST) * C::TILE_BYTES;
   #pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
+                for (int kk = kk0; kk < kk1; ++kk)
                   mma_ts(d_o, a_p + kk * 8, desc_mnmajor<D>(v_s, kk), idesc_o, (np[q] > 0 || kk > 0) ? 1u : 0u);
               }
+            };
+            if (jv < sp[q] && jv < v_ready && !half[q] &&
+                mbar_probe(bar((DROP ? C::B_PHALF : C::B_PFULL) + q), np[q] & 1)) {
+              tc_fence_after_sync();
+              issue_pv(std::integral_constant<int, 0>{}, KK_FIRST{});
+              if constexpr (DROP) {
+                half[q] = true;
+              } else {
+                tc_commit(bar(C::B_ODONE + q));
+                pp[q] = jv + 1;
+                ++np[q];
+              }
+              progress = true;
+            }
+            if (DROP && half[q] && mbar_probe(bar(C::B_PFULL + q), np[q] & 1)) {
+              tc_fence_after_sync();
+              issue_pv(std::integral_constant<int, C::BN / 32>{}, KK_ALL{});
               tc_commit(bar(C::B_ODONE + q));
               pp[q] = jv + 1;
               ++np[q];
+              half[q] = false;
               progress = true;
             }
             // S_q at sp
@@ -584,7 +609,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         }
       }
     };
-    if (nk > 0) draw_tile(0);  // dropout is dense: tile j starts at key j * 128
+    // The key tile of this tile's first position (block-sparse: the first it uses).
+    if (DROP && nk > 0) {
+      int p0 = 0;
+      if constexpr (SPARSE)
+        while (!uses(q, p0)) ++p0;
+      draw_tile(kv_tile(p0) * C::BN);
+    }
     // K/V stage release: stage p % NST of position p may be refilled once the
     // MMAs of both tiles that read it have completed.  Each position's empty
     // barrier takes two arrival units: one from each tile that uses it, or
@@ -770,7 +801,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       tmem_st_wait();
       tc_fence_before_sync();
       mbar_arrive(bar(C::B_PFULL + q));
-      if (DROP && j + 1 < nk) draw_tile((j + 1) * C::BN);
+      if (DROP && j + 1 < nk) {  // the key tile of this tile's next position
+        int pn = pj + 1;
+        if constexpr (SPARSE)
+          while (!uses(q, pn)) ++pn;
+        draw_tile(kv_tile(pn) * C::BN);
+      }
       prev_p = pj;
     }
     // ------------------------------------------------------------ epilogue
@@ -864,8 +900,16 @@ int launch_fwd_t(const FwdArgs& a) {
 }  // namespace
 
 int launch_fwd(const FwdArgs& a) {
-  if (a.drop.t != 0) {  // dropout: dense
-    if (a.bmask) return kStatusUnsupported;
+  if (a.drop.t != 0 && a.bmask) {  // dropout under a block mask
+    if ((a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
+    switch (a.d) {
+      case 32: return a.bf16 ? launch_fwd_t<32, true, true, true>(a) : launch_fwd_t<32, false, true, true>(a);
+      case 64: return a.bf16 ? launch_fwd_t<64, true, true, true>(a) : launch_fwd_t<64, false, true, true>(a);
+      case 128: return a.bf16 ? launch_fwd_t<128, true, true, true>(a) : launch_fwd_t<128, false, true, true>(a);
+      default: return kStatusUnsupported;
+    }
+  }
+  if (a.drop.t != 0) {  // dropout
     switch (a.d) {
       case 32: return a.bf16 ? launch_fwd_t<32, true, false, true>(a) : launch_fwd_t<32, false, false, true>(a);
       case 64: return a.bf16 ? launch_fwd_t<64, true, false, true>(a) : launch_fwd_t<64, false, false, true>(a);

@@ -66,10 +66,15 @@ def _load():
                                             P, P, ctypes.c_int]
         lib.oracle_cols_dropout.argtypes = [P, P, P, P, P, P, I64, I64, I64, D, ctypes.c_int, D, U64, U32, P, P,
                                             I64, P, P, ctypes.c_int]
+        lib.oracle_forward_masked_dropout.argtypes = [P, P, P, P, P, P, I64, I64, I64, D, ctypes.c_int, P, I64,
+                                                      I64, D, U64, U32, ctypes.c_int]
+        lib.oracle_backward_masked_dropout.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I64, D, ctypes.c_int, P,
+                                                       I64, I64, D, U64, U32, ctypes.c_int]
         for f in (lib.oracle_forward, lib.oracle_backward, lib.oracle_rows, lib.oracle_cols,
                   lib.oracle_forward_masked, lib.oracle_backward_masked, lib.oracle_dropout_keep,
                   lib.oracle_forward_dropout, lib.oracle_backward_dropout, lib.oracle_rows_dropout,
-                  lib.oracle_cols_dropout):
+                  lib.oracle_cols_dropout, lib.oracle_forward_masked_dropout,
+                  lib.oracle_backward_masked_dropout):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -125,12 +130,10 @@ def dropout_keep(p, seed, offset, bh, n_rows, n_cols):
     return out
 
 
-def _drop(dropout, block_mask):
+def _drop(dropout):
     """dropout = (p, seed, offset) or None."""
     if dropout is None:
         return None
-    if block_mask is not None:
-        raise ValueError("dropout and block_mask are not combined")
     p, seed, offset = dropout
     return float(p), int(seed), int(offset)
 
@@ -142,7 +145,8 @@ def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None,
     block_mask: optional [H or 1, nb, nb] (nb = ceil(N/blk)); key j is hidden
     from query i unless block_mask[h][i // blk][j // blk] is nonzero.
     dropout: optional (p, seed, offset): inverted dropout on P (P returned
-    by want_p is the softmax before dropout; LSE is undropped).
+    by want_p is the softmax before dropout; LSE is undropped); with a
+    block_mask too, the keep rule applies to the keys the mask leaves visible.
     Returns (o [B,H,N,d], lse [B,H,N]) or (o, lse, p [B,H,N,N]).
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
@@ -151,8 +155,12 @@ def forward(q, k, v, scale, causal, want_p=False, threads=None, block_mask=None,
     lse = np.empty((B, H, N), dtype=np.float64)
     p = np.empty((B, H, N, N), dtype=np.float64) if want_p else None
     m, mh = _mask(block_mask, H, N, blk)
-    dr = _drop(dropout, block_mask)
-    if dr is not None:
+    dr = _drop(dropout)
+    if dr is not None and m is not None:
+        rc = _load().oracle_forward_masked_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H,
+                                                   N, d, float(scale), int(bool(causal)), _ptr(m), mh, blk, *dr,
+                                                   threads or default_threads())
+    elif dr is not None:
         rc = _load().oracle_forward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(p), B * H, N, d,
                                             float(scale), int(bool(causal)), *dr, threads or default_threads())
     elif m is None:
@@ -174,8 +182,13 @@ def backward(q, k, v, o, do, scale, causal, threads=None, block_mask=None, blk=1
     B, H, N, d = _shape(q)
     dq, dk, dv = np.empty_like(q), np.empty_like(q), np.empty_like(q)
     m, mh = _mask(block_mask, H, N, blk)
-    dr = _drop(dropout, block_mask)
-    if dr is not None:
+    dr = _drop(dropout)
+    if dr is not None and m is not None:
+        rc = _load().oracle_backward_masked_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq),
+                                                    _ptr(dk), _ptr(dv), B * H, N, d, float(scale),
+                                                    int(bool(causal)), _ptr(m), mh, blk, *dr,
+                                                    threads or default_threads())
+    elif dr is not None:
         rc = _load().oracle_backward_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(dq), _ptr(dk),
                                              _ptr(dv), B * H, N, d, float(scale), int(bool(causal)), *dr,
                                              threads or default_threads())
@@ -205,7 +218,7 @@ def rows(q, k, v, do, scale, causal, bh_idx, row_idx, threads=None, dropout=None
     o = np.empty((n, d), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     dq = np.empty((n, d), dtype=np.float64) if do is not None else None
-    dr = _drop(dropout, None)
+    dr = _drop(dropout)
     if dr is not None:
         rc = _load().oracle_rows_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(do), B * H, N, d, float(scale),
                                          int(bool(causal)), *dr, _ptr(bh), _ptr(ri), n, _ptr(o), _ptr(lse), _ptr(dq),
@@ -231,7 +244,7 @@ def cols(q, k, v, do, lse_all, D_all, scale, causal, bh_idx, col_idx, threads=No
     n = bh.shape[0]
     dk = np.empty((n, d), dtype=np.float64)
     dv = np.empty((n, d), dtype=np.float64)
-    dr = _drop(dropout, None)
+    dr = _drop(dropout)
     if dr is not None:
         rc = _load().oracle_cols_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(lse_all), _ptr(D_all), B * H, N,
                                          d, float(scale), int(bool(causal)), *dr, _ptr(bh), _ptr(ci), n, _ptr(dk),

@@ -318,6 +318,19 @@ int oracle_forward_dropout(const double *q, const double *k, const double *v, do
   return forward_job(q, k, v, o, lse, p_out, BH, N, d, scale, causal, NULL, 0, 0, &dr, nthreads);
 }
 
+/* Block mask and dropout together: key j reaches O_i with weight
+ * P_ij * keep_ij * 256 / t when it is visible (mask and causal rule), 0
+ * otherwise; P is the softmax over the visible keys, before dropout. */
+int oracle_forward_masked_dropout(const double *q, const double *k, const double *v, double *o,
+                                  double *lse, double *p_out, int64_t BH, int64_t N, int64_t d,
+                                  double scale, int causal, const uint8_t *bmask, int64_t mask_heads,
+                                  int64_t blk, double p, uint64_t seed, uint32_t offset, int nthreads) {
+  drop_t dr;
+  if (!bmask || drop_init(&dr, p, seed, offset)) return 1;
+  return forward_job(q, k, v, o, lse, p_out, BH, N, d, scale, causal, bmask, mask_heads, blk, &dr,
+                     nthreads);
+}
+
 int oracle_forward(const double *q, const double *k, const double *v, double *o, double *lse,
                    double *p_out, int64_t BH, int64_t N, int64_t d, double scale, int causal,
                    int nthreads) {
@@ -443,6 +456,19 @@ int oracle_backward_dropout(const double *q, const double *k, const double *v, c
   drop_t dr;
   if (drop_init(&dr, p, seed, offset)) return 1;
   return backward_job(q, k, v, o, dO, dq, dk, dv, BH, N, d, scale, causal, NULL, 0, 0, &dr,
+                      nthreads);
+}
+
+/* Backward of oracle_forward_masked_dropout (o its output for the same mask,
+ * p, seed and offset). */
+int oracle_backward_masked_dropout(const double *q, const double *k, const double *v, const double *o,
+                                   const double *dO, double *dq, double *dk, double *dv, int64_t BH,
+                                   int64_t N, int64_t d, double scale, int causal, const uint8_t *bmask,
+                                   int64_t mask_heads, int64_t blk, double p, uint64_t seed,
+                                   uint32_t offset, int nthreads) {
+  drop_t dr;
+  if (!bmask || drop_init(&dr, p, seed, offset)) return 1;
+  return backward_job(q, k, v, o, dO, dq, dk, dv, BH, N, d, scale, causal, bmask, mask_heads, blk, &dr,
                       nthreads);
 }
 

@@ -1,6 +1,6 @@
 """The differentiable wrapper gives exactly what the C entry points give:
 O from attn_fwd and, through loss.backward(), the gradients of attn_bwd
-(and of the dropout pair), bit for bit."""
+(and of the dropout and block-mask pairs), bit for bit."""
 import math
 
 import pytest
@@ -40,5 +40,28 @@ def test_autograd_matches_the_entry_points(pkg, causal, p_drop):
     assert pkg.sync_status() == 0
     assert torch.equal(o.detach(), o_ref)
     # dK and dV bit for bit; dQ is reduced with atomics in any order
+    assert torch.equal(kk.grad, g[1]) and torch.equal(vv.grad, g[2])
+    assert (qq.grad.float() - g[0].float()).abs().max().item() <= 1e-2 * g[0].float().abs().max().item()
+
+
+@pytest.mark.parametrize("p_drop", [0.0, 0.3])
+def test_autograd_with_a_block_mask(pkg, p_drop):
+    x = make_inputs(AttnShape(1, 2, 700, 128), "bf16", seed=33)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    g0 = torch.Generator().manual_seed(2)
+    mask = (torch.rand((2, 6, 6), generator=g0) < 0.5).to(torch.uint8)
+    mask[:, torch.arange(6), torch.arange(6)] = 1
+    mask = mask.cuda()
+    qq, kk, vv = (t.clone().requires_grad_(True) for t in (q, k, v))
+    o = pkg.attention(qq, kk, vv, scale=0.09, causal=True, dropout_p=p_drop, seed=11, offset=5, block_mask=mask)
+    (o.float() * do.float()).sum().backward()
+    if p_drop > 0:
+        o_ref, lse = pkg.attn_fwd_blocksparse_dropout(q, k, v, mask, p_drop, 11, 5, scale=0.09, causal=True)
+        g = pkg.attn_bwd_blocksparse_dropout(q, k, v, o_ref, do, lse, mask, p_drop, 11, 5, scale=0.09, causal=True)
+    else:
+        o_ref, lse = pkg.attn_fwd_blocksparse(q, k, v, mask, scale=0.09, causal=True)
+        g = pkg.attn_bwd_blocksparse(q, k, v, o_ref, do, lse, mask, scale=0.09, causal=True)
+    assert pkg.sync_status() == 0
+    assert torch.equal(o.detach(), o_ref)
     assert torch.equal(kk.grad, g[1]) and torch.equal(vv.grad, g[2])
     assert (qq.grad.float() - g[0].float()).abs().max().item() <= 1e-2 * g[0].float().abs().max().item()

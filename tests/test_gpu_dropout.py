@@ -85,14 +85,17 @@ def run(x, scale, causal, drop):
     return o, lse, grads
 
 
-def check_full(x, scale, causal, drop, o, lse, grads):
+def check_full(x, scale, causal, drop, o, lse, grads, block_mask=None):
     d32 = (float(np.float32(drop[0])), drop[1], drop[2])
     q, k, v, do = (f64(x[n]) for n in ("q", "k", "v", "do"))
-    oo, lo, P = oracle.forward(q, k, v, scale, causal, want_p=True, dropout=d32)
+    bm = None if block_mask is None else block_mask.cpu().numpy()
+    oo, lo, P = oracle.forward(q, k, v, scale, causal, want_p=True, block_mask=bm, dropout=d32)
     err = np.abs(f64(o) - oo)
     assert (err - half_ulp(oo, o.dtype)).max() <= TOL_O, "max|dO| %g" % err.max()
-    assert np.abs(f64(lse) - lo).max() <= TOL_LSE
-    ref = oracle.backward(q, k, v, oo, do, scale, causal, dropout=d32)
+    empty = np.isneginf(lo)  # rows that see no key (block mask): LSE = -inf, O = 0
+    assert np.array_equal(np.isneginf(f64(lse)), empty)
+    assert np.abs(f64(lse)[~empty] - lo[~empty]).max() <= TOL_LSE
+    ref = oracle.backward(q, k, v, oo, do, scale, causal, block_mask=bm, dropout=d32)
     floor = 1e-3 * float(np.linalg.norm(do))
     delta = (np.abs(do) * 2 * half_ulp(oo, o.dtype)).sum(-1)  # [B, H, N]
     extra = {"dq": abs(scale) * delta[..., None] * (P @ np.abs(k)),
@@ -254,3 +257,123 @@ def test_bad_probability_is_rejected():
         pkg.attn_fwd_dropout(q.float(), k.float(), v.float(), 0.1, 1, 0)
     with pytest.raises(TypeError):  # one type for all inputs
         pkg.attn_fwd_dropout(q, k.half(), v, 0.1, 1, 0)
+
+
+# ---------------------------------------------------------------------------
+# Dropout under a block mask (attn_fwd_blocksparse_dropout and its backward):
+# the keep decisions are those above, applied to the keys the mask leaves
+# visible; skipped key tiles shift which key tile a CTA visits next, so the
+# draws must follow the tile actually visited.
+
+def run_sparse(x, mask, scale, causal, drop):
+    pkg = _pkg()
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    m = mask.cuda()
+    p, seed, off = drop
+    o, lse = pkg.attn_fwd_blocksparse_dropout(q, k, v, m, p, seed, off, scale=scale, causal=causal)
+    grads = pkg.attn_bwd_blocksparse_dropout(q, k, v, o, do, lse, m, p, seed, off, scale=scale, causal=causal)
+    assert pkg.sync_status() == 0
+    return o, lse, grads
+
+
+def _sparse_mask(heads, nb, density, seed):
+    g = torch.Generator().manual_seed(seed)
+    m = (torch.rand((heads, nb, nb), generator=g) < density).to(torch.uint8)
+    m[:, torch.arange(nb), torch.arange(nb)] = 1
+    m[0, 1, :] = 0  # query block 1 of head 0 sees no key
+    m[:, :, nb - 1] = 0  # no query block sees the last key block
+    return m
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocksparse_full(d, causal):
+    N = 1000  # 8 tiles, the last one ragged
+    x = make_inputs(AttnShape(1, 3, N, d), "bf16", seed=90 + d)
+    mask = _sparse_mask(3, 8, 0.4, seed=d + causal)
+    drop = (0.5, 0x5EED_0000_0000_0001 + d, 7)
+    o, lse, grads = run_sparse(x, mask, 1 / math.sqrt(d), causal, drop)
+    check_full(x, 1 / math.sqrt(d), causal, drop, o, lse, grads, block_mask=mask)
+
+
+def test_blocksparse_fp16_full():
+    x = make_inputs(AttnShape(2, 2, 600, 64), "fp16", seed=97)
+    mask = _sparse_mask(1, 5, 0.5, seed=3)
+    for causal in (False, True):
+        drop = (0.2, 4242, causal)
+        o, lse, grads = run_sparse(x, mask, 0.125, causal, drop)
+        assert o.dtype == torch.float16 and grads[0].dtype == torch.float16
+        check_full(x, 0.125, causal, drop, o, lse, grads, block_mask=mask)
+
+
+def _two_per_row_mask(H, nb, seed):
+    """Every query block sees exactly two key blocks (so every row has the
+    same 256 visible keys), chosen at random per head."""
+    g = np.random.default_rng(seed)
+    m = np.zeros((H, nb, nb), dtype=np.uint8)
+    for h in range(H):
+        for r in range(nb):
+            m[h, r, g.choice(nb, 2, replace=False)] = 1
+    return torch.from_numpy(m)
+
+
+def test_blocksparse_keep_mask_is_bit_exact():
+    """The forward and backward readbacks above under a block mask with two
+    key blocks per query block: O_ic = (256/t)/256 sum_m keep_i,128m+c
+    vis 2^m and dV_jc = (256/t)/256 sum_m keep_128m+c,j vis 2^m, so every
+    keep decision of a visible pair is read back as a bit."""
+    B, H, N, d = 1, 3, 512, 128
+    nb = N // 128
+    p, seed, off = 0.45, 0xABCDEF_12345678, 21
+    t = threshold(p)
+    mask = _two_per_row_mask(H, nb, seed=12)
+    mnp = mask.numpy().astype(np.int64)
+    q = torch.zeros(B, H, N, d, dtype=torch.bfloat16, device="cuda")
+    k = make_inputs(AttnShape(B, H, N, d), "bf16", seed=15)["k"].cuda()
+    j = torch.arange(N)
+    unit = torch.zeros(N, d)
+    unit[j, j % 128] = torch.exp2((j // 128).float())
+    unit = unit.expand(B, H, N, d).contiguous().to(torch.bfloat16).cuda()
+    pkg = _pkg()
+    m = mask.cuda()
+    o, lse = pkg.attn_fwd_blocksparse_dropout(q, k, unit, m, p, seed, off, scale=0.1)
+    _, _, dv = pkg.attn_bwd_blocksparse_dropout(q, k, unit, o, unit, lse, m, p, seed, off, scale=0.1)
+    assert pkg.sync_status() == 0
+    np.testing.assert_allclose(f64(lse)[0], math.log(256.0), atol=1e-5)
+    o, dv = f64(o), f64(dv)
+    for h in range(H):
+        keep = oracle.dropout_keep(float(np.float32(p)), seed, off, h, N, N).astype(np.int64)  # [query, key]
+        vis = np.kron(mnp[h], np.ones((128, 128), dtype=np.int64))
+        kv = keep * vis
+        cnt = _decode_counts(o[0, h], 256.0, t)  # [N queries, 128]
+        np.testing.assert_array_equal(cnt, sum(kv[:, 128 * b:128 * (b + 1)] << b for b in range(nb)))
+        cnt = _decode_counts(dv[0, h], 256.0, t)  # [N keys, 128]
+        kt = kv.T
+        np.testing.assert_array_equal(cnt, sum(kt[:, 128 * b:128 * (b + 1)] << b for b in range(nb)))
+
+
+def test_blocksparse_all_ones_equals_dropout_kernels():
+    """With every tile enabled the block-sparse kernels visit the tiles of the
+    dense ones in the same order: the forward is bit-identical; the backward
+    as in the block-sparse tests without dropout (dK, dV bit-identical under
+    the causal mask, to one bf16 ulp without it; dQ to rounding)."""
+    x = make_inputs(AttnShape(1, 2, 900, 128), "bf16", seed=31)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    mask = torch.ones((1, 8, 8), dtype=torch.uint8, device="cuda")
+    pkg = _pkg()
+    drop = (0.25, 555, 3)
+    for causal in (False, True):
+        o1, l1 = pkg.attn_fwd_dropout(q, k, v, *drop, scale=0.1, causal=causal)
+        o2, l2 = pkg.attn_fwd_blocksparse_dropout(q, k, v, mask, *drop, scale=0.1, causal=causal)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
+        g1 = pkg.attn_bwd_dropout(q, k, v, o1, do, l1, *drop, scale=0.1, causal=causal)
+        g2 = pkg.attn_bwd_blocksparse_dropout(q, k, v, o1, do, l1, mask, *drop, scale=0.1, causal=causal)
+        if causal:
+            assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+        else:
+            for a, b in ((g1[1], g2[1]), (g1[2], g2[2])):
+                a, b = a.float(), b.float()
+                ulp = torch.exp2(torch.floor(torch.log2(b.abs().clamp_min(1e-30))) - 7)
+                assert ((a - b).abs() <= ulp + 1e-6 * b.abs().max()).all()
+        assert (g1[0].float() - g2[0].float()).abs().max().item() <= 1e-2 * g1[0].float().abs().max().item()
+    assert pkg.sync_status() == 0

@@ -174,3 +174,93 @@ def test_dropout_rejects_bad_probability():
     for p in (1.0, -0.1, float("nan"), 0.999):
         with pytest.raises(RuntimeError):
             oracle.forward(x["q"], x["k"], x["v"], 0.5, False, dropout=(p, 1, 1))
+
+
+# ---------------------------------------------------------------------------
+# Dropout under a block mask.  The keep rule is the one pinned above and does
+# not depend on the mask; the mask decides which keys enter the softmax
+# (FlashAttention深度攻略 §7 fuses both into the softmax step; 进阶追问
+# "Sparse FlashAttention" is the block mask).
+
+def _block_mask(H, nb, density, seed):
+    m = (np.random.default_rng(seed).random((H, nb, nb)) < density).astype(np.uint8)
+    m[0, 1, :] = 0  # query block 1 of head 0 sees no key
+    m[:, :, nb - 1] = 0  # no query block sees the last key block
+    m[:, 0, 0] = 1
+    return m
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_masked_dropout_reads_every_weight(causal):
+    """V_j = e_j turns O_i into the weights themselves: key j contributes
+    (256/t) keep_ij / n_i when it is visible and nothing otherwise, where n_i
+    counts the visible keys of row i (Q = 0 makes their P equal); a row with
+    no visible key gives O = 0 and LSE = -inf."""
+    N, blk, p, seed, offset = 23, 4, 0.4, 77, 9
+    nb = (N + blk - 1) // blk
+    H = 2
+    mask = _block_mask(H, nb, 0.5, seed=3)
+    t = _threshold(p)
+    q = np.zeros((1, H, N, N))
+    k = np.random.default_rng(2).standard_normal((1, H, N, N))
+    v = np.broadcast_to(np.eye(N), (1, H, N, N)).copy()
+    o, lse = oracle.forward(q, k, v, 0.3, causal, block_mask=mask, blk=blk, dropout=(p, seed, offset))
+    for h in range(H):
+        keep = oracle.dropout_keep(p, seed, offset, h, N, N)
+        for i in range(N):
+            vis = np.array([bool(mask[h, i // blk, j // blk]) and (not causal or j <= i) for j in range(N)])
+            n = vis.sum()
+            if n == 0:
+                assert np.all(o[0, h, i] == 0) and lse[0, h, i] == -np.inf
+                continue
+            np.testing.assert_allclose(o[0, h, i], (256.0 / t) * (vis & (keep[i] == 1)) / n, rtol=1e-13, atol=0)
+            assert lse[0, h, i] == pytest.approx(math.log(n), rel=1e-14)
+    assert np.any(lse == -np.inf)  # the empty query block is exercised
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_masked_dropout_special_cases(causal):
+    """An all-ones mask gives the dropout oracle and p = 0 gives the block-mask
+    oracle, bit for bit."""
+    x = _np_inputs(1, 2, 37, 8, seed=21)
+    nb = (37 + 7) // 8
+    ones = np.ones((1, nb, nb), dtype=np.uint8)
+    drop = (0.25, 99, 1)
+    a = oracle.forward(x["q"], x["k"], x["v"], 0.4, causal, block_mask=ones, blk=8, dropout=drop)
+    b = oracle.forward(x["q"], x["k"], x["v"], 0.4, causal, dropout=drop)
+    assert all(np.array_equal(u, w) for u, w in zip(a, b))
+    ga = oracle.backward(x["q"], x["k"], x["v"], a[0], x["do"], 0.4, causal, block_mask=ones, blk=8, dropout=drop)
+    gb = oracle.backward(x["q"], x["k"], x["v"], b[0], x["do"], 0.4, causal, dropout=drop)
+    assert all(np.array_equal(u, w) for u, w in zip(ga, gb))
+    mask = _block_mask(2, nb, 0.5, seed=8)
+    c = oracle.forward(x["q"], x["k"], x["v"], 0.4, causal, block_mask=mask, blk=8, dropout=(0.0, 5, 5))
+    e = oracle.forward(x["q"], x["k"], x["v"], 0.4, causal, block_mask=mask, blk=8)
+    assert all(np.array_equal(u, w) for u, w in zip(c, e))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_masked_dropout_backward_matches_finite_differences(causal):
+    rng = np.random.default_rng(60 + causal)
+    N, d, blk = 20, 2, 4
+    q, k, v, do = (rng.standard_normal((1, 1, N, d)) for _ in range(4))
+    mask = _block_mask(1, N // blk, 0.6, seed=4)
+    drop = (0.3, 31337, 2)
+    o, _ = oracle.forward(q, k, v, 0.9, causal, block_mask=mask, blk=blk, dropout=drop)
+    dq, dk, dv = oracle.backward(q, k, v, o, do, 0.9, causal, block_mask=mask, blk=blk, dropout=drop)
+    assert np.all(dk[0, 0, -blk:] == 0) and np.all(dv[0, 0, -blk:] == 0)  # the key block no query sees
+
+    def loss(qq, kk, vv):
+        oo, _ = oracle.forward(qq, kk, vv, 0.9, causal, threads=1, block_mask=mask, blk=blk, dropout=drop)
+        return float((oo * do).sum())
+
+    h = 1e-6
+    for name, grad in (("q", dq), ("k", dk), ("v", dv)):
+        base = {"q": q, "k": k, "v": v}
+        fd = np.zeros_like(grad)
+        for idx in np.ndindex(*grad.shape):
+            plus = {n: a.copy() for n, a in base.items()}
+            minus = {n: a.copy() for n, a in base.items()}
+            plus[name][idx] += h
+            minus[name][idx] -= h
+            fd[idx] = (loss(plus["q"], plus["k"], plus["v"]) - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-8, err_msg=name)
