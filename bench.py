@@ -432,6 +432,51 @@ def measure_dropout(attn, steps, warmup, peaks, p_drop=0.1):
     return res
 
 
+def measure_small_d(attn, steps, warmup, peaks):
+    """The head-dimension-64 shapes: the GPT-2 shape (B=8 H=12 N=1024 d=64,
+    causal) and B=2 H=16 N=8192 d=64 (non-causal), forward and whole backward
+    call (preprocess + main + dQ conversion), FLOPs as for the main workload.
+    Inputs fit in L2 at the GPT-2 shape (38 MB); the number is a warm-L2 one."""
+    import torch
+    from io_aware_exact_12_gb300.synth import AttnShape, make_inputs
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    res = {}
+    for key, (B, H, N, d, causal) in (("gpt2_shape_causal", (8, 12, 1024, 64, True)),
+                                      ("n8192_d64", (2, 16, 8192, 64, False))):
+        x = make_inputs(AttnShape(B, H, N, d), "bf16", seed=4)
+        q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        g = [torch.empty_like(q) for _ in range(3)]
+        f_fwd, f_bwd = flops_per_step(B, H, N, d, causal)
+
+        def fwd():
+            attn.attn_fwd(q, k, v, causal=causal, o=o, lse=lse)
+
+        def bwd():
+            attn.attn_bwd(q, k, v, o, do, lse, causal=causal, dq=g[0], dk=g[1], dv=g[2])
+
+        r = {"workload": "B=%d H=%d N=%d d=%d bf16, %s" % (B, H, N, d, "causal" if causal else "non-causal")}
+        for name, fn, fl in (("fwd", fwd, f_fwd), ("bwd", bwd, f_bwd)):
+            for _ in range(max(warmup, 3)):
+                fwd()
+                fn()
+            torch.cuda.synchronize()
+            n = max(steps, 20)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n
+            tf = fl / (ms * 1e-3) / 1e12
+            r[name] = {"ms": ms, "tflops": tf, "frac": tf / peak}
+        res[key] = r
+    res["status"] = attn.sync_status()
+    return res
+
+
 def bench_config(world):
     """The `config` of both arms' lines (the same dict, so the two compare)."""
     return dict(WORKLOAD, parallelism="dp%d (independent heads per rank)" % world)
@@ -712,6 +757,7 @@ def run_ours(args):
     fp8 = measure_fp8(attn, K, args.warmup, peaks) if rank == 0 else None
     sparse = measure_blocksparse(attn, K, args.warmup, peaks) if rank == 0 else None
     dropout = measure_dropout(attn, K, args.warmup, peaks) if rank == 0 else None
+    small_d = measure_small_d(attn, K, args.warmup, peaks) if rank == 0 else None
     exp_bound = measure_exp_bound(attn, B, H, N, fwd_ms, bwd_ms) if rank == 0 else None
 
     cpu = None
@@ -732,7 +778,7 @@ def run_ours(args):
                            "fwd_tflops": cf_f / (statistics.median(cf_ms) * 1e-3) / 1e12,
                            "bwd_tflops": cb_f / (statistics.median(cb_ms) * 1e-3) / 1e12},
                 "roofline": roof, "cpu_baseline": cpu, "decode": decode, "fp8": fp8, "blocksparse": sparse,
-                "dropout": dropout, "exp_bound": exp_bound,
+                "dropout": dropout, "d64": small_d, "exp_bound": exp_bound,
                 "e2e": {"value": e2e_value, "unit": UNIT, "ms_per_step": e2e_ms,
                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                         "pipeline": ("%d head-chunks: copies in / compute (%d streams) / copies out overlapped; "
