@@ -34,12 +34,13 @@
 //   * TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
 //     P_q overwrites half of S_q, and the tile's next S goes out right after
 //     the current P V (the tensor pipe runs one thread's MMAs in issue order).
-// At d <= 64 a CTA holds ONE query tile (NQ = 1: warps 0-3 softmax, 4 the
-// producer, 5 the issuer; 256 TMEM columns S, O, P; a 2-stage ring) and two
-// CTAs share each SM, so the tile-to-tile overlap comes from the other CTA,
-// which also hides this CTA's set-up, first loads, drain and epilogue (and a
-// block-sparse CTA walks its own tile's list, not the union of two).  P has
-// TMEM columns of its own there, so a tile's next S goes out once its
+// At d <= 64, and for block-sparse masks at d = 128, a CTA holds ONE query
+// tile (NQ = 1: warps 0-3 softmax, 4 the producer, 5 the issuer; 256 TMEM
+// columns; a 2-stage ring at d <= 64, 1 stage at d = 128) and two CTAs share
+// each SM, so the tile-to-tile overlap comes from the other CTA, which also
+// hides this CTA's set-up, first loads, drain and epilogue, and a
+// block-sparse CTA walks its own tile's list, not the union of two.  At
+// d <= 64 P has TMEM columns of its own, so a tile's next S goes out once its
 // softmax has read the current S.
 // Causal: key tiles entirely above the diagonal are never loaded or
 // multiplied; only the diagonal tile (and the ragged last tile) are masked;
@@ -66,9 +67,9 @@ constexpr float kRescaleThresholdLog2 = 8.0f;
 // where CTAs of one query tile use half the TMEM, a third less shared memory
 // and half the softmax warps, so that two of them share an SM and one's
 // set-up, first loads, drain and epilogue overlap the other's steps.
-template <int D, int NQ = 2, bool DROP = false>
+template <int D, int NQ = 2, bool DROP = false, bool SPARSE = false>
 struct FwdCfg {
-  static_assert(NQ == 2 || (NQ == 1 && D <= 64), "one-tile CTAs exist for d <= 64 only");
+  static_assert(NQ == 1 || NQ == 2, "one or two query tiles per CTA");
   static constexpr int BM = 128;                     // query rows per tile (MMA M)
   static constexpr int BN = 128;                     // key rows per tile
   static constexpr int ROWB = (D >= 64) ? 128 : 64;  // bytes per swizzled row
@@ -78,7 +79,8 @@ struct FwdCfg {
   static constexpr int SBO = 8 * ROWB;               // bytes between 8-row groups
   static constexpr int CHUNK_BYTES = 128 * ROWB;     // one column chunk of a 128-row tile
   static constexpr int TILE_BYTES = 128 * D * 2;
-  static constexpr int NST = (D == 128 || NQ == 1) ? 2 : 3;
+  // (one-tile CTAs at d = 128: a single stage, so that two CTAs fit an SM)
+  static constexpr int NST = (NQ == 1 && D == 128) ? 1 : (D == 128 || NQ == 1) ? 2 : 3;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + NST * TILE_BYTES;
@@ -109,10 +111,13 @@ struct FwdCfg {
   static constexpr int MIN_BLOCKS = 3 - NQ;       // CTAs per SM
   // 65536 / (THREADS * MIN_BLOCKS), rounded down to a multiple of 8: 168, or 128 for one-tile CTAs
   static constexpr int REGS_LAUNCH = (65536 / (THREADS * MIN_BLOCKS)) & ~7;
-  // softmax warpgroups / producer and MMA warpgroup (one-tile CTAs: the
-  // dropout softmax, which carries a tile of draws, takes 16 more)
-  static constexpr int REGS_MATH = NQ == 2 ? 224 : (DROP ? 224 : 208);
-  static constexpr int REGS_CTRL = NQ == 2 ? 56 : (DROP ? 32 : 48);
+  // softmax warpgroups / producer and MMA warpgroup.  One-tile CTAs split
+  // 256 a thread: 208 / 48; with dropout (a tile of draws carried by the
+  // softmax) 224 / 32; block-sparse at d = 128 (the list-walking issuer)
+  // 200 / 56 -- each the fastest of the splits measured for its variant
+  // (224 / 32 and 208 / 48 measured 14 % and 6 % slower than 200 / 56 there).
+  static constexpr int REGS_MATH = NQ == 2 ? 224 : DROP ? 224 : (SPARSE && D == 128) ? 200 : 208;
+  static constexpr int REGS_CTRL = NQ == 2 ? 56 : DROP ? 32 : (SPARSE && D == 128) ? 56 : 48;
   static_assert(NQ * 128 * REGS_MATH + 128 * REGS_CTRL <= THREADS * REGS_LAUNCH, "register split");
   static constexpr uint32_t TMEM_COLS = NQ == 2 ? 512 : 256;
   // At d <= 64, P_q has TMEM columns of its own after O0, O1 (64 columns of
@@ -185,14 +190,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // walk positions, so a K/V tile is loaded once per CTA and each query tile
 // runs its S/PV chain over its own positions only.
 template <int D, bool BF16, bool SPARSE, bool DROP, int NQ>
-__global__ void __launch_bounds__(FwdCfg<D, NQ, DROP>::THREADS, FwdCfg<D, NQ, DROP>::MIN_BLOCKS)
+__global__ void __launch_bounds__(FwdCfg<D, NQ, DROP, SPARSE>::THREADS, FwdCfg<D, NQ, DROP, SPARSE>::MIN_BLOCKS)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, uint8_t* __restrict__ o_out,
                     float* __restrict__ lse_out, int N, float sl2, int causal, int negate,
                     const uint8_t* __restrict__ bmask, int H, int mask_heads, int* status,
                     DropParams drop, int head_group) {
-  using C = FwdCfg<D, NQ, DROP>;
+  using C = FwdCfg<D, NQ, DROP, SPARSE>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -894,7 +899,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ, DROP>::THREADS, FwdCfg<D, NQ, DR
 
 template <int D, bool BF16, bool SPARSE, bool DROP = false, int NQ = 2>
 int launch_fwd_t(const FwdArgs& a) {
-  using C = FwdCfg<D, NQ, DROP>;
+  using C = FwdCfg<D, NQ, DROP, SPARSE>;
   CUtensorMap mq, mk, mv;
   const int rowb = C::ROWB;
   if (!encode_bhnd_map(&mq, a.q, a.BH, a.N, D, C::CH, 128, rowb, BF16) ||
@@ -913,27 +918,29 @@ int launch_fwd_t(const FwdArgs& a) {
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }
 
+// Query tiles per CTA: one (two CTAs per SM) at d <= 64 and for block-sparse
+// masks at d = 128, where a CTA then walks its own tile's key list; two for
+// the plain and dropout forward at d = 128 (one-tile CTAs measured mixed
+// there, and the dropout softmax needs the two-tile CTA's registers).
+template <int D>
+int launch_fwd_d(const FwdArgs& a) {
+  const bool sparse = a.bmask != nullptr, drop = a.drop.t != 0;
+  constexpr int NQ = D == 128 ? 2 : 1;
+  if (sparse && drop)
+    return a.bf16 ? launch_fwd_t<D, true, true, true, NQ>(a) : launch_fwd_t<D, false, true, true, NQ>(a);
+  if (drop) return a.bf16 ? launch_fwd_t<D, true, false, true, NQ>(a) : launch_fwd_t<D, false, false, true, NQ>(a);
+  if (sparse) return a.bf16 ? launch_fwd_t<D, true, true, false, 1>(a) : launch_fwd_t<D, false, true, false, 1>(a);
+  return a.bf16 ? launch_fwd_t<D, true, false, false, NQ>(a) : launch_fwd_t<D, false, false, false, NQ>(a);
+}
+
 }  // namespace
 
 int launch_fwd(const FwdArgs& a) {
-  // d <= 64: CTAs of one query tile, two per SM (measured faster at every
-  // sequence length); d = 128: two query tiles per CTA.
   if (a.bmask && (a.N + 127) / 128 > kMaxSparseTiles) return kStatusUnsupported;
-  const bool sparse = a.bmask != nullptr, drop = a.drop.t != 0;
   switch (a.d) {
-#define ATTN_FWD_CASE(DD, NQQ)                                                                       \
-  case DD:                                                                                           \
-    if (sparse && drop)                                                                              \
-      return a.bf16 ? launch_fwd_t<DD, true, true, true, NQQ>(a) : launch_fwd_t<DD, false, true, true, NQQ>(a); \
-    if (drop)                                                                                        \
-      return a.bf16 ? launch_fwd_t<DD, true, false, true, NQQ>(a) : launch_fwd_t<DD, false, false, true, NQQ>(a); \
-    if (sparse)                                                                                      \
-      return a.bf16 ? launch_fwd_t<DD, true, true, false, NQQ>(a) : launch_fwd_t<DD, false, true, false, NQQ>(a); \
-    return a.bf16 ? launch_fwd_t<DD, true, false, false, NQQ>(a) : launch_fwd_t<DD, false, false, false, NQQ>(a);
-    ATTN_FWD_CASE(32, 1)
-    ATTN_FWD_CASE(64, 1)
-    ATTN_FWD_CASE(128, 2)
-#undef ATTN_FWD_CASE
+    case 32: return launch_fwd_d<32>(a);
+    case 64: return launch_fwd_d<64>(a);
+    case 128: return launch_fwd_d<128>(a);
     default: return kStatusUnsupported;
   }
 }
