@@ -129,3 +129,16 @@ def test_blocksparse_backward_rejects_bad_arguments(L):
     assert L.attn_bwd_blocksparse(*a, None, 1, 1, 2, 256, 128, 0.1, 0, None) == 1       # no mask
     assert L.attn_bwd_blocksparse(*a, FAKE, 3, 1, 2, 256, 128, 0.1, 0, None) == 1       # mask_heads not 1 or H
     assert L.attn_bwd_blocksparse(*a, FAKE, 1, 1, 2, 262144 + 128, 128, 0.1, 0, None) == 2  # > 2048 tiles
+
+
+def test_blocksparse_dropout_rejects_bad_arguments(L):
+    fa = [FAKE + i * 0x100000 for i in range(5)]
+    assert L.attn_fwd_blocksparse_dropout(*fa, None, 1, 1, 2, 256, 128, 0.1, 0, 0.1, 1, 0, None) == 1   # no mask
+    assert L.attn_fwd_blocksparse_dropout(*fa, FAKE, 3, 1, 2, 256, 128, 0.1, 0, 0.1, 1, 0, None) == 1   # mask_heads
+    assert L.attn_fwd_blocksparse_dropout(*fa, FAKE, 1, 1, 2, 256, 128, 0.1, 0, 1.0, 1, 0, None) == 1   # p_drop
+    assert L.attn_fwd_blocksparse_dropout_f16(*fa, FAKE, 1, 1, 2, 256, 96, 0.1, 0, 0.1, 1, 0, None) == 2  # d
+    a = [FAKE + i * 0x100000 for i in range(9)]
+    assert L.attn_bwd_blocksparse_dropout(*a, None, 1, 1, 2, 256, 128, 0.1, 0, 0.1, 1, 0, None) == 1
+    assert L.attn_bwd_blocksparse_dropout(*a, FAKE, 1, 1, 2, 256, 128, 0.1, 0, -0.5, 1, 0, None) == 1
+    assert L.attn_bwd_blocksparse_dropout_f16(*a, FAKE, 1, 1, 2, 262144 + 128, 128, 0.1, 0, 0.1, 1, 0,
+                                              None) == 2  # > 2048 tiles
