@@ -96,6 +96,34 @@ def test_block_diagonal_mask(pkg):
     _check(pkg, AttnShape(1, 2, N, 128), mask, False, seed=9)
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("N", [1, 127, 129])
+def test_small_and_ragged_sequences(pkg, N, d):
+    """One and two query tiles, the last one ragged: a CTA's single tile, its
+    one- or two-entry key list and the tail mask (forward and backward)."""
+    nb = (N + 127) // 128
+    for causal in (False, True):
+        mask = _random_mask(2, nb, 0.5, seed=N * d + causal)
+        _check(pkg, AttnShape(1, 2, N, d), mask, causal, seed=N + d)
+        _check_bwd(pkg, AttnShape(1, 2, N, d), mask, causal, seed=N + d + 1)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_all_zero_mask(pkg, d):
+    """No key visible anywhere: O = 0 and LSE = -inf in every row, all
+    gradients exactly zero, and nothing is loaded."""
+    N = 300
+    nb = (N + 127) // 128
+    x = make_inputs(AttnShape(1, 2, N, d), "bf16", seed=13)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    mask = torch.zeros((1, nb, nb), dtype=torch.uint8, device="cuda")
+    o, lse = pkg.attn_fwd_blocksparse(q, k, v, mask, scale=0.1)
+    dq, dk, dv = pkg.attn_bwd_blocksparse(q, k, v, o, do, lse, mask, scale=0.1)
+    assert pkg.sync_status() == 0
+    assert not o.any() and torch.isneginf(lse).all()
+    assert not dq.any() and not dk.any() and not dv.any()
+
+
 def test_sparse_long_sequence_sampled_rows(pkg):
     """N = 8192 with a 25 %-dense mask: sampled rows against the oracle's
     definition on the visible keys of each row (rows of the masked problem)."""
