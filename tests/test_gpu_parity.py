@@ -243,6 +243,27 @@ def test_causal_order_short_last_head_group(N):
     _check_identities(x, grads)
 
 
+# The same with one-tile CTAs (d = 64): the forward groups 128 MB / (4 N d
+# bytes) = 16 heads at N = 32768, so 20 heads make 16 and 4; the backward 2
+# heads a group.
+def test_causal_order_one_tile_ctas():
+    pkg = _pkg()
+    x = make_inputs(AttnShape(1, 20, 32768, 64), "bf16", seed=16)
+    s = 1.0 / math.sqrt(64)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), device="cuda")
+    pkg.attn_fwd(q, k, v, scale=s, causal=True, o=o, lse=lse)
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    pkg.attn_bwd(q, k, v, o, do, lse, scale=s, causal=True, dq=dq, dk=dk, dv=dv)
+    assert pkg.sync_status() == 0
+    for t in (o, lse, dq, dk, dv):
+        assert torch.isfinite(t).all()
+    grads = (dq, dk, dv)
+    _check_sampled(x, s, True, o, lse, grads, nrows=256, heads_for_cols=[19], ncols=32)
+    _check_identities(x, grads)
+
+
 # ------------------------------------------------------------- edge cases
 @pytest.mark.parametrize("N", [1, 2, 63, 127, 129, 255, 257, 383])
 @pytest.mark.parametrize("d", [32, 64, 128])
