@@ -603,6 +603,7 @@ def run_ours(args):
     f_fwd, f_bwd = flops_per_step(B, H, N, d, causal)
     value = world * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
     launches = K * 4
+    dv_ref_last = dv.view(B * H, N, d)[-1].clone()  # the timed steps' dV of the last head (checks e2e below)
 
     # causal variant of the same workload (reported alongside, not in `value`),
     # timed like the main step: back-to-back steps, one synchronisation at the end
@@ -645,7 +646,11 @@ def run_ours(args):
     # computes (E2E_COMPUTE_STREAMS compute streams in turn, so one chunk's
     # kernels can fill the SMs the previous chunk's leave idle at their tail) and
     # chunk c-1's results are copied out (stream s_out).  Every input byte is
-    # copied in and every result byte copied out inside the step.
+    # copied in and every result byte copied out inside the step.  The pinned
+    # host buffers hold each chunk's q, k, v, dO (and o, dq, dk, dv) next to one
+    # another, so a chunk moves in one copy and out in two (o/dq/dk/dv, lse),
+    # and the per-chunk tensors and events are made once, outside the timed
+    # region: the host's work per step stays well below the GPU's.
     BH = B * H
     nch = args.e2e_chunks if args.e2e_chunks > 0 and BH % args.e2e_chunks == 0 else 1
     hc = BH // nch
@@ -655,56 +660,51 @@ def run_ours(args):
     def flat(t):
         return t.view(BH, *t.shape[2:])
 
+    IN_NAMES, OUT_NAMES = ("q", "k", "v", "do"), ("o", "dq", "dk", "dv")
+    hin_pk = torch.empty((nch, 4, hc, N, d), dtype=q.dtype, pin_memory=True)
+    for j, n in enumerate(IN_NAMES):
+        hin_pk[:, j].copy_(flat(hin[n]).view(nch, hc, N, d))
     # Two sets of device buffers (and of pinned host outputs): step i uses set
     # i % 2, so step i+1's input copies overlap step i's compute and copies out,
     # and step i+2 waits for step i to have finished with the set.
-    dev_sets, hst_sets = [], []
+    sets = []
     for sidx in range(2):
-        if sidx == 0:
-            dv_t = {"q": q, "k": k, "v": v, "do": do, "o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-            ho = hout
-        else:
-            dv_t = {n: torch.empty_like(t) for n, t in (("q", q), ("k", k), ("v", v), ("do", do), ("o", o),
-                                                        ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-            ho = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in hout.items()}
-        dev_sets.append({n: flat(t) for n, t in dv_t.items()})
-        hst_sets.append({n: flat(t) for n, t in list(hin.items()) + list(ho.items())})
+        din = torch.empty((nch, 4, hc, N, d), dtype=q.dtype, device=q.device)
+        dout = torch.empty((nch, 4, hc, N, d), dtype=q.dtype, device=q.device)
+        dlse = torch.empty((nch, hc, N), dtype=lse.dtype, device=q.device)
+        hout_pk = torch.empty((nch, 4, hc, N, d), dtype=q.dtype, pin_memory=True)
+        hlse = torch.empty((nch, hc, N), dtype=lse.dtype, pin_memory=True)
+        views = [{**{n: din[c, j].unsqueeze(0) for j, n in enumerate(IN_NAMES)},
+                  **{n: dout[c, j].unsqueeze(0) for j, n in enumerate(OUT_NAMES)},
+                  "lse": dlse[c].unsqueeze(0)} for c in range(nch)]
+        sets.append({"din": din, "dout": dout, "dlse": dlse, "hout": hout_pk, "hlse": hlse, "views": views,
+                     "ev_in": [torch.cuda.Event() for _ in range(nch)],
+                     "ev_cmp": [torch.cuda.Event() for _ in range(nch)], "done": torch.cuda.Event()})
 
     def e2e_step(start_ev, sidx=0):
-        dev, hst = dev_sets[sidx], hst_sets[sidx]
-        ev_in, ev_cmp = [], []
+        st = sets[sidx]
         s_in.wait_event(start_ev)
         with torch.cuda.stream(s_in):
             for c in range(nch):
-                sl = slice(c * hc, (c + 1) * hc)
-                for n in ("q", "k", "v", "do"):
-                    dev[n][sl].copy_(hst[n][sl], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s_in)
-                ev_in.append(e)
+                st["din"][c].copy_(hin_pk[c], non_blocking=True)
+                st["ev_in"][c].record(s_in)
         for c in range(nch):
             sc = s_cmp[c % len(s_cmp)]
-            sc.wait_event(ev_in[c])
-            sl = slice(c * hc, (c + 1) * hc)
-            cq, ck, cv, cdo = (dev[n][sl].unsqueeze(0) for n in ("q", "k", "v", "do"))
-            co, cl = dev["o"][sl].unsqueeze(0), dev["lse"][sl].unsqueeze(0)
+            sc.wait_event(st["ev_in"][c])
+            w = st["views"][c]
             with torch.cuda.stream(sc):
-                attn.attn_fwd(cq, ck, cv, scale=scale, causal=causal, o=co, lse=cl)
-                attn.attn_bwd(cq, ck, cv, co, cdo, cl, scale=scale, causal=causal, dq=dev["dq"][sl].unsqueeze(0),
-                              dk=dev["dk"][sl].unsqueeze(0), dv=dev["dv"][sl].unsqueeze(0))
-                e = torch.cuda.Event()
-                e.record(sc)
-                ev_cmp.append(e)
+                attn.attn_fwd(w["q"], w["k"], w["v"], scale=scale, causal=causal, o=w["o"], lse=w["lse"])
+                attn.attn_bwd(w["q"], w["k"], w["v"], w["o"], w["do"], w["lse"], scale=scale, causal=causal,
+                              dq=w["dq"], dk=w["dk"], dv=w["dv"])
+                st["ev_cmp"][c].record(sc)
         with torch.cuda.stream(s_out):
             for c in range(nch):
-                s_out.wait_event(ev_cmp[c])
-                sl = slice(c * hc, (c + 1) * hc)
-                for n in ("o", "lse", "dq", "dk", "dv"):
-                    hst[n][sl].copy_(dev[n][sl], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(s_out)
-        stream.wait_event(done)
-        return done
+                s_out.wait_event(st["ev_cmp"][c])
+                st["hout"][c].copy_(st["dout"][c], non_blocking=True)
+                st["hlse"][c].copy_(st["dlse"][c], non_blocking=True)
+        st["done"].record(s_out)
+        stream.wait_event(st["done"])
+        return st["done"]
 
     def time_e2e(fn, sets):
         # With one buffer set each step starts after the previous one has
@@ -731,9 +731,15 @@ def run_ours(args):
     e2e_ms = time_e2e(e2e_step, 2)
     e2e_value = world * (f_fwd + f_bwd) / (e2e_ms * 1e-3) / 1e12
     launches_e2e = K * 4 * nch
-    # the pipelined steps' results are the same numbers (dV has no atomics):
-    # check the last head of both host output sets against the device result
-    e2e_check = all(bool(torch.equal(h["dv"][-1].cuda(), dv.view(BH, N, d)[-1])) for h in hst_sets[:min(2, K)])
+    # Checks on the last head's dV (no atomics in dV): each host copy equals the
+    # device buffer it was copied from, both buffer sets hold the same numbers,
+    # and they equal the timed steps' dV to rounding (a chunk of 4 heads makes
+    # a grid without the full grid's split last wave, so the fp32 partial sums
+    # of the split key tiles associate differently).
+    last = [st["hout"][nch - 1, 3, hc - 1] for st in sets[:min(2, K)]]
+    e2e_check = (all(bool(torch.equal(h.cuda(), st["dout"][nch - 1, 3, hc - 1])) for h, st in zip(last, sets))
+                 and all(bool(torch.equal(h, last[0])) for h in last)
+                 and bool(torch.allclose(last[0].cuda().float(), dv_ref_last.float(), rtol=1e-2, atol=1e-3)))
     seq_ms = time_e2e(lambda ev, sidx: e2e_step_sequential(), 1)  # one stream: already serialised
 
     peaks, peak_src = load_peaks()
