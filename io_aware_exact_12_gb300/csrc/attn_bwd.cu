@@ -173,6 +173,8 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(
     const uint8_t* __restrict__ o, const uint8_t* __restrict__ dO, const float* __restrict__ lse,
     float* __restrict__ lse2, float* __restrict__ dvec, float* __restrict__ dq_acc, int N, int Npad,
     int64_t rows_total) {
+  griddep_wait();  // (launch_serialized)
+  griddep_launch_dependents();
   // lse2 receives -LSE * log2(e) and dvec receives -D, the forms the main pass adds.
   constexpr int PER = D / 8;  // elements per lane (8 lanes per row)
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -244,6 +246,8 @@ __global__ void __launch_bounds__(256) attn_dq_convert_kernel(const float* __res
                                                               int split_from, int nkt, int N,
                                                               uint8_t* __restrict__ dk,
                                                               uint8_t* __restrict__ dv) {
+  griddep_wait();  // (launch_serialized)
+  griddep_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   for (int64_t g = tid; g < groups; g += stride) {
@@ -300,6 +304,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                     float sl2, float scale, int causal, int negate, int* status,
                     DropParams drop, const uint8_t* __restrict__ bmask, int H, int mask_heads,
                     int head_group, int BH, int split_from, float* __restrict__ part) {
+  // (always launched normally: any overlap code here measured 0.3-1.6 % slower
+  // at N = 8192, this kernel being sensitive to its code layout)
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -855,12 +861,16 @@ int launch_bwd_t(const BwdArgs& a) {
   auto kern = attn_bwd_kernel<D, BF16, DROP, SPARSE>;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
+  // the preprocess and the dQ conversion overlap their neighbours' tails when
+  // the main grid is short (one CTA per SM)
+  const bool overlap = overlap_launches(static_cast<int64_t>((a.N + C::BN - 1) / C::BN) * a.BH, 1);
   {
     const int64_t threads = rows_total * 8;
     const int blocks = static_cast<int>((threads + 255) / 256);
-    attn_bwd_pre_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(
-        static_cast<const uint8_t*>(a.o), static_cast<const uint8_t*>(a.dO), a.lse, a.ws_lse2,
-        a.ws_d, a.ws_dq, a.N, Npad, rows_total);
+    if (launch_serialized(overlap, attn_bwd_pre_kernel<D, BF16>, dim3(blocks), dim3(256), 0, a.stream,
+                          static_cast<const uint8_t*>(a.o), static_cast<const uint8_t*>(a.dO), a.lse, a.ws_lse2,
+                          a.ws_d, a.ws_dq, a.N, Npad, rows_total) != cudaSuccess)
+      return kStatusCuda;
   }
   // One block per (key tile, head) item, head after head; the last tail_split
   // items (no causal mask, no block mask) as two half-range blocks each.
@@ -869,17 +879,21 @@ int launch_bwd_t(const BwdArgs& a) {
   const int tail = (SPARSE || a.causal || !a.ws_part) ? 0 : a.tail_split;
   if (items + tail > 0x7fffffff) return kStatusUnsupported;
   const int split_from = static_cast<int>(items - tail);
-  kern<<<static_cast<unsigned>(items + tail), C::THREADS, C::SMEM_BYTES, a.stream>>>(
-      mq, mk, mv, mdo, a.ws_lse2, a.ws_d, a.ws_dq, static_cast<uint8_t*>(a.dk),
-      static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status, a.drop,
-      a.bmask, a.H, a.mask_heads, order_head_group(a.BH, int64_t{8} * a.N * D, int64_t{32} << 20), a.BH,
-      split_from, a.ws_part);
+  if (launch_serialized(false, kern, dim3(static_cast<unsigned>(items + tail)), dim3(C::THREADS), C::SMEM_BYTES,
+                        a.stream,
+                        mq, mk, mv, mdo, a.ws_lse2, a.ws_d, a.ws_dq, static_cast<uint8_t*>(a.dk),
+                        static_cast<uint8_t*>(a.dv), a.N, Npad, a.sl2, a.scale, a.causal, a.negate, a.status,
+                        a.drop, a.bmask, a.H, a.mask_heads,
+                        order_head_group(a.BH, int64_t{8} * a.N * D, int64_t{32} << 20), a.BH, split_from,
+                        a.ws_part) != cudaSuccess)
+    return kStatusCuda;
   {
     const int64_t groups = static_cast<int64_t>(a.BH) * a.N * D / 8;
     const int blocks = static_cast<int>(std::min<int64_t>((groups + 255) / 256, 152 * 16));
-    attn_dq_convert_kernel<D, BF16><<<blocks, 256, 0, a.stream>>>(
-        a.ws_dq, static_cast<uint8_t*>(a.dq), groups, a.ws_part, tail, split_from, nkt, a.N,
-        static_cast<uint8_t*>(a.dk), static_cast<uint8_t*>(a.dv));
+    if (launch_serialized(overlap, attn_dq_convert_kernel<D, BF16>, dim3(blocks), dim3(256), 0, a.stream, a.ws_dq,
+                          static_cast<uint8_t*>(a.dq), groups, a.ws_part, tail, split_from, nkt, a.N,
+                          static_cast<uint8_t*>(a.dk), static_cast<uint8_t*>(a.dv)) != cudaSuccess)
+      return kStatusCuda;
   }
   return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
 }

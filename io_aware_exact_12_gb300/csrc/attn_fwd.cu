@@ -196,9 +196,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ, DROP, SPARSE>::THREADS, FwdCfg<D
                     const __grid_constant__ CUtensorMap tm_v, uint8_t* __restrict__ o_out,
                     float* __restrict__ lse_out, int N, float sl2, int causal, int negate,
                     const uint8_t* __restrict__ bmask, int H, int mask_heads, int* status,
-                    DropParams drop, int head_group) {
+                    DropParams drop, int head_group, int overlap) {
   using C = FwdCfg<D, NQ, DROP, SPARSE>;
   extern __shared__ __align__(1024) uint8_t smem[];
+  if (overlap) {  // launched overlapped (launch_serialized)
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int bh = blockIdx.y, qb = blockIdx.x;
@@ -911,11 +915,13 @@ int launch_fwd_t(const FwdArgs& a) {
   // The warpgroup register split adds up only at this launch allocation.
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
   dim3 grid((a.N + NQ * C::BM - 1) / (NQ * C::BM), a.BH);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mv, static_cast<uint8_t*>(a.o), a.lse,
-                                                      a.N, a.sl2, a.causal, a.negate, a.bmask, a.H,
-                                                      a.mask_heads, a.status, a.drop,
-                                                      order_head_group(a.BH, int64_t{4} * a.N * D, int64_t{128} << 20));
-  return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
+  const bool overlap = overlap_launches(static_cast<int64_t>(grid.x) * grid.y, C::MIN_BLOCKS);
+  const cudaError_t e = launch_serialized(overlap, kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, mq, mk, mv,
+                                          static_cast<uint8_t*>(a.o), a.lse, a.N, a.sl2, a.causal, a.negate,
+                                          a.bmask, a.H, a.mask_heads, a.status, a.drop,
+                                          order_head_group(a.BH, int64_t{4} * a.N * D, int64_t{128} << 20),
+                                          overlap ? 1 : 0);
+  return e == cudaSuccess ? kStatusOk : kStatusCuda;
 }
 
 // Query tiles per CTA: one (two CTAs per SM) at d <= 64 and for block-sparse

@@ -36,6 +36,14 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 
 // Makes mbarrier initialisation visible to the async proxy (TMA, tcgen05).
+// Programmatic dependent launch (launch_serialized): the first instructions of
+// every kernel of the attention passes.  griddep_wait returns once the grid
+// this one was launched behind has completed and its memory is visible (at
+// once for a normal launch); griddep_launch_dependents lets the next such
+// launch in the stream start placing its blocks, which then wait in turn.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
