@@ -64,6 +64,8 @@ template <int D>
 __global__ void __launch_bounds__(kDecThreads) attn_decode_split_kernel(
     const uint8_t* __restrict__ q, const uint8_t* __restrict__ k, const uint8_t* __restrict__ v,
     float* __restrict__ part, int L, int keys_per_split, float sl2) {
+  griddep_wait();  // launched overlapped (launch_serialized)
+  griddep_launch_dependents();
   using V = DecVec<D>;
   constexpr int E = V::E;
   const int s = blockIdx.x, bh = blockIdx.y, S = gridDim.x;
@@ -167,6 +169,8 @@ template <int D>
 __global__ void __launch_bounds__(128) attn_decode_merge_kernel(const float* __restrict__ part,
                                                                 uint8_t* __restrict__ o,
                                                                 float* __restrict__ lse, int S) {
+  griddep_wait();  // launched overlapped (launch_serialized)
+  griddep_launch_dependents();
   const int bh = blockIdx.x;
   const float* p = part + static_cast<size_t>(bh) * S * (D + 2);
   float mm = -INFINITY;
@@ -192,11 +196,18 @@ template <int D>
 int launch_decode_t(const DecodeArgs& a) {
   const int S = a.splits;
   const int kps = (a.L + S - 1) / S;
-  attn_decode_split_kernel<D><<<dim3(S, a.BH), kDecThreads, 0, a.stream>>>(
-      static_cast<const uint8_t*>(a.q), static_cast<const uint8_t*>(a.k),
-      static_cast<const uint8_t*>(a.v), a.ws, a.L, kps, a.sl2);  // sl2 = scale*log2(e), signed
-  attn_decode_merge_kernel<D><<<a.BH, 128, 0, a.stream>>>(a.ws, static_cast<uint8_t*>(a.o), a.lse, S);
-  return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
+  // Both launches overlap their predecessor's tail (a decode step is short,
+  // so the launch latency is a visible share of it); each kernel waits for
+  // its predecessor before reading anything.
+  if (launch_serialized(true, attn_decode_split_kernel<D>, dim3(S, a.BH), dim3(kDecThreads), 0, a.stream,
+                        static_cast<const uint8_t*>(a.q), static_cast<const uint8_t*>(a.k),
+                        static_cast<const uint8_t*>(a.v), a.ws, a.L, kps,
+                        a.sl2) != cudaSuccess)  // sl2 = scale*log2(e), signed
+    return kStatusCuda;
+  return launch_serialized(true, attn_decode_merge_kernel<D>, dim3(a.BH), dim3(128), 0, a.stream, a.ws,
+                           static_cast<uint8_t*>(a.o), a.lse, S) == cudaSuccess
+             ? kStatusOk
+             : kStatusCuda;
 }
 
 }  // namespace
