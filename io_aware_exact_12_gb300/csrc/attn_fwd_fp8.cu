@@ -116,6 +116,8 @@ __device__ __forceinline__ void drain_wait8(uint32_t bar, uint32_t parity) {
 __global__ void __launch_bounds__(256) attn_fp8_transpose_kernel(const uint8_t* __restrict__ v,
                                                                   uint8_t* __restrict__ vt, int N,
                                                                   int Npad) {
+  griddep_wait();  // launched overlapped (launch_serialized)
+  griddep_launch_dependents();
   __shared__ uint8_t tile[128][128 + 16];
   const int kb = blockIdx.x, bh = blockIdx.y;
   const uint8_t* src = v + (static_cast<size_t>(bh) * N + static_cast<size_t>(kb) * 128) * 128;
@@ -143,10 +145,14 @@ __global__ void __launch_bounds__(Fp8Cfg::THREADS, 1)
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_vt, uint8_t* __restrict__ o_out,
                         float* __restrict__ lse_out, int N, float sl2, float descale_v, int causal,
-                        int* status, int head_group) {
+                        int* status, int head_group, int overlap) {
   using C = Fp8Cfg;
   constexpr int D = C::D;
   extern __shared__ __align__(1024) uint8_t smem[];
+  if (overlap) {  // launched overlapped (launch_serialized)
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int bh = blockIdx.y, qb = blockIdx.x;
@@ -469,8 +475,12 @@ int launch_fwd_fp8(const Fp8Args& a) {
   using C = Fp8Cfg;
   if (a.d != 128) return kStatusUnsupported;
   const int Npad = ((a.N + 127) / 128) * 128;
-  attn_fp8_transpose_kernel<<<dim3(Npad / 128, a.BH), 256, 0, a.stream>>>(
-      static_cast<const uint8_t*>(a.v), a.ws_vt, a.N, Npad);
+  // both launches overlap their predecessor's tail on grids of at most 8 waves
+  dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
+  const bool overlap = overlap_launches(static_cast<int64_t>(grid.x) * grid.y, 1);
+  if (launch_serialized(overlap, attn_fp8_transpose_kernel, dim3(Npad / 128, a.BH), dim3(256), 0, a.stream,
+                        static_cast<const uint8_t*>(a.v), a.ws_vt, a.N, Npad) != cudaSuccess)
+    return kStatusCuda;
   CUtensorMap mq, mk, mvt;
   if (!encode_map_u8(&mq, a.q, 128, a.N, a.BH, 128, static_cast<uint64_t>(a.N) * 128, 128, 128) ||
       !encode_map_u8(&mk, a.k, 128, a.N, a.BH, 128, static_cast<uint64_t>(a.N) * 128, 128, 128) ||
@@ -479,11 +489,12 @@ int launch_fwd_fp8(const Fp8Args& a) {
   auto kern = attn_fwd_fp8_kernel;
   if (!ensure_smem_attr(reinterpret_cast<const void*>(kern), C::SMEM_BYTES)) return kStatusCuda;
   if (!check_launch_regs(reinterpret_cast<const void*>(kern), C::REGS_LAUNCH)) return kStatusDeviceCheck;
-  dim3 grid((a.N + 2 * C::BM - 1) / (2 * C::BM), a.BH);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(mq, mk, mvt, static_cast<uint8_t*>(a.o), a.lse, a.N,
-                                                      a.sl2, a.descale_v, a.causal, a.status,
-                                                      order_head_group(a.BH, int64_t{2} * a.N * C::D, int64_t{128} << 20));
-  return cudaGetLastError() == cudaSuccess ? kStatusOk : kStatusCuda;
+  return launch_serialized(overlap, kern, grid, dim3(C::THREADS), C::SMEM_BYTES, a.stream, mq, mk, mvt,
+                           static_cast<uint8_t*>(a.o), a.lse, a.N, a.sl2, a.descale_v, a.causal, a.status,
+                           order_head_group(a.BH, int64_t{2} * a.N * C::D, int64_t{128} << 20),
+                           overlap ? 1 : 0) == cudaSuccess
+             ? kStatusOk
+             : kStatusCuda;
 }
 
 }  // namespace attn
